@@ -1,0 +1,280 @@
+"""Pins for the fp64 oracle: facts fixed by mathematics, not by the oracle itself.
+
+Each ``check_*`` raises AssertionError on a mismatch and takes an oracle
+handle, so the negative controls at the bottom can run the same checks on
+copies of the oracle compiled with a deliberate mistake.
+
+Operation (LightLLM PR #1703, PR description): per 64-token chunk and head,
+``(I + A)^-1`` for the strictly lower-triangular chunk matrix ``A``; chunks
+restart at every request start (packed) or batch row (dense).
+"""
+from __future__ import annotations
+
+import itertools
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import kda_inputs as ki
+import oracle as orc_mod
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_cases.txt")
+BT = 64
+
+
+def _series_inverse(M: np.ndarray) -> np.ndarray:
+    """(I + M)^-1 = sum_{k=0}^{n-1} (-M)^k, exact for nilpotent (strictly lower) M."""
+    n = M.shape[0]
+    term = np.eye(n)
+    acc = np.eye(n)
+    for _ in range(1, n):
+        term = term @ (-M)
+        acc = acc + term
+    return acc
+
+
+def _strict(M: np.ndarray, n: int) -> np.ndarray:
+    out = np.tril(np.asarray(M, dtype=np.float64)[:n, :n], -1)
+    return out
+
+
+def _load_golden():
+    cases = []
+    lines = [l.strip() for l in open(GOLDEN) if l.strip() and not l.startswith("#")]
+    i = 0
+    while i < len(lines):
+        assert lines[i].startswith("case")
+        name = lines[i].split()[1]
+        n = int(lines[i + 1].split()[1])
+        assert lines[i + 2] == "M"
+        M = np.array([[float(x) for x in lines[i + 3 + r].split()] for r in range(n)])
+        assert lines[i + 3 + n] == "X"
+        X = np.array([[float(x) for x in lines[i + 4 + n + r].split()] for r in range(n)])
+        assert lines[i + 4 + 2 * n] == "end"
+        cases.append((name, n, M, X))
+        i += 5 + 2 * n
+    return cases
+
+
+# ---------------------------------------------------------------- the checks
+
+def check_golden(orc):
+    """Hand-worked cases from tests/golden/worked_cases.txt, bit-exact."""
+    for name, n, M, X in _load_golden():
+        got = orc.invert_chunk(M, n)
+        assert np.array_equal(got[:n, :n], X), name
+        assert np.array_equal(got[n:, n:], np.eye(BT - n)), name
+
+
+def check_worked_small(orc):
+    """2x2 [[0,0],[a,0]] -> [[1,0],[-a,1]]; 4x4 bidiagonal a=2 -> (-2)^(i-j)."""
+    for a in (0.5, -3.0, 7.25):
+        got = orc.invert_chunk(np.array([[0.0, 0.0], [a, 0.0]]), 2)
+        assert np.array_equal(got[:2, :2], np.array([[1.0, 0.0], [-a, 1.0]]))
+    M = np.diag([2.0] * 3, -1)
+    got = orc.invert_chunk(M, 4)
+    want = np.array([[(-2.0) ** (i - j) if j <= i else 0.0 for j in range(4)] for i in range(4)])
+    assert np.array_equal(got[:4, :4], want)
+
+
+def _cofactor_inverse(L):
+    """Exact inverse of an integer unit lower-triangular matrix via cofactors (Leibniz)."""
+    n = len(L)
+
+    def det(m):
+        k = len(m)
+        if k == 0:
+            return Fraction(1)
+        tot = Fraction(0)
+        for perm in itertools.permutations(range(k)):
+            inv = sum(1 for a in range(k) for b in range(a + 1, k) if perm[a] > perm[b])
+            p = Fraction(-1 if inv % 2 else 1)
+            for r in range(k):
+                p *= m[r][perm[r]]
+                if p == 0:
+                    break
+            tot += p
+        return tot
+
+    d = det(L)
+    X = [[Fraction(0)] * n for _ in range(n)]
+    for i in range(n):
+        for j in range(n):
+            minor = [[L[r][c] for c in range(n) if c != i] for r in range(n) if r != j]
+            X[i][j] = (-1) ** (i + j) * det(minor) / d
+    return X
+
+
+def check_rational(orc):
+    """Small-integer cases, n <= 6, equal exactly to the cofactor inverse in rationals."""
+    rng = np.random.default_rng(1234)
+    for n in range(1, 7):
+        for _ in range(3):
+            M = np.tril(rng.integers(-3, 4, size=(n, n)), -1).astype(np.float64)
+            L = [[Fraction(int(M[r][c])) + (1 if r == c else 0) for c in range(n)] for r in range(n)]
+            X = _cofactor_inverse(L)
+            want = np.array([[float(x) for x in row] for row in X])
+            got = orc.invert_chunk(M, n)
+            assert np.array_equal(got[:n, :n], want), (n, M)
+
+
+def check_closed_form(orc):
+    """Config-style, no-decay and Gaussian chunks against the nilpotent series, 1e-12."""
+    for kind, seed in (("kda", 11), ("nodecay", 12), ("gauss", 13)):
+        wl = ki.Workload("pin", "packed", H=2, in_dtype="f32", out_dtype="f32", seed=seed,
+                         seqlens=(64, 40, 17), kind=kind)
+        inp = ki.build(wl)
+        A = orc_mod.to_f64(inp.A)[0]
+        for row0, n in inp.chunks():
+            for h in range(inp.H):
+                M = _strict(A[row0:row0 + n, h, :], n)
+                want = _series_inverse(M)
+                got = orc.invert_chunk(A[row0:row0 + n, h, :], n)[:n, :n]
+                err = np.abs(got - want) / (1.0 + np.abs(want))
+                assert err.max() <= 1e-12, (kind, row0, n, h, err.max())
+
+
+def check_exact_64(orc):
+    """64x64 structures whose inverse is exact in floating point."""
+    Z = np.zeros((BT, BT))
+    I = np.eye(BT)
+    assert np.array_equal(orc.invert_chunk(Z, BT), I)
+    ones = np.tril(np.ones((BT, BT)), -1)
+    assert np.array_equal(orc.invert_chunk(ones, BT), I - np.diag(np.ones(BT - 1), -1))
+    bi = np.diag(np.full(BT - 1, 0.5), -1)
+    want = np.array([[(-0.5) ** (i - j) if j <= i else 0.0 for j in range(BT)] for i in range(BT)])
+    assert np.array_equal(orc.invert_chunk(bi, BT), want)
+    rng = np.random.default_rng(7)
+    # nonzeros only in the four diagonal 16x16 blocks: off-diagonal blocks stay exactly 0
+    M = np.zeros((BT, BT))
+    for b in range(4):
+        s = slice(16 * b, 16 * b + 16)
+        M[s, s] = np.tril(rng.standard_normal((16, 16)) * 0.3, -1)
+    X = orc.invert_chunk(M, BT)
+    for bi_ in range(4):
+        for bj in range(4):
+            blk = X[16 * bi_:16 * bi_ + 16, 16 * bj:16 * bj + 16]
+            if bi_ != bj:
+                assert np.all(blk == 0.0)
+            else:
+                want = _series_inverse(M[16 * bi_:16 * bi_ + 16, 16 * bi_:16 * bi_ + 16])
+                assert np.abs(blk - want).max() <= 1e-13
+    # nonzeros only in one off-diagonal block: A^2 = 0, so the inverse is I - A exactly
+    for p in range(4):
+        for q in range(p):
+            M = np.zeros((BT, BT))
+            M[16 * p:16 * p + 16, 16 * q:16 * q + 16] = rng.standard_normal((16, 16))
+            assert np.array_equal(orc.invert_chunk(M, BT), I - M), (p, q)
+    # chains of blocks with power-of-two entries: I - A + A^2 - A^3 exactly
+    for chain in ([(1, 0), (2, 1)], [(1, 0), (2, 1), (3, 2)], [(2, 1), (3, 2)], [(3, 1), (1, 0)]):
+        M = np.zeros((BT, BT))
+        for p, q in chain:
+            M[16 * p:16 * p + 16, 16 * q:16 * q + 16] = (
+                rng.integers(-1, 2, size=(16, 16)) * 2.0 ** -rng.integers(0, 4, size=(16, 16)))
+        want = I - M + M @ M - M @ M @ M
+        assert np.array_equal(orc.invert_chunk(M, BT), want), chain
+
+
+def check_residual(orc):
+    """||(I + M) X - I||_max <= 1e-12 on config-style chunks, full and partial."""
+    wl = ki.Workload("pin", "dense", H=3, in_dtype="f32", out_dtype="f32", seed=21, B=2, T=100)
+    inp = ki.build(wl)
+    A = orc_mod.to_f64(inp.A).reshape(-1, inp.H, BT)
+    for row0, n in inp.chunks():
+        for h in range(inp.H):
+            M = _strict(A[row0:row0 + n, h, :], n)
+            X = orc.invert_chunk(A[row0:row0 + n, h, :], n)[:n, :n]
+            assert np.abs((np.eye(n) + M) @ X - np.eye(n)).max() <= 1e-12
+
+
+def _expected_layout(A64, chunks, H):
+    """Per-chunk placement written out independently of the oracle's own enumeration."""
+    out = np.zeros_like(A64)
+    for row0, n in chunks:
+        for h in range(H):
+            M = _strict(A64[row0:row0 + n, h, :], n)
+            X = _series_inverse(M)
+            out[row0:row0 + n, h, :n] = X
+    return out
+
+
+def check_layout(orc):
+    """Chunk boundaries: packed restarts at each request, dense at each batch row."""
+    wl = ki.Workload("pin", "packed", H=2, in_dtype="f32", out_dtype="f32", seed=31,
+                     seqlens=(5, 70, 64, 0, 130, 1), kind="gauss")
+    inp = ki.build(wl)
+    A = orc_mod.to_f64(inp.A)
+    got = orc.solve_tril(A, inp.cu_seqlens.numpy())[0]
+    want = _expected_layout(A[0], inp.chunks(), inp.H)
+    assert np.abs(got - want).max() <= 1e-12
+    # each request solved alone as a dense row gives the same bits
+    cu = inp.cu_seqlens.tolist()
+    for s in range(len(cu) - 1):
+        if cu[s + 1] == cu[s]:
+            continue
+        dense = orc.solve_tril(A[:, cu[s]:cu[s + 1]])
+        assert np.array_equal(dense[0], got[cu[s]:cu[s + 1]])
+    wl = ki.Workload("pin", "dense", H=2, in_dtype="f32", out_dtype="f32", seed=32, B=3, T=77,
+                     kind="gauss")
+    inp = ki.build(wl)
+    A = orc_mod.to_f64(inp.A)
+    got = orc.solve_tril(A).reshape(-1, inp.H, BT)
+    want = _expected_layout(A.reshape(-1, inp.H, BT), inp.chunks(), inp.H)
+    assert np.abs(got - want).max() <= 1e-12
+
+
+def check_poison(orc):
+    """NaN written into every ignored element changes nothing."""
+    wl = ki.Workload("pin", "packed", H=2, in_dtype="f32", out_dtype="f32", seed=41,
+                     seqlens=(3, 64, 100))
+    clean = ki.build(wl)
+    dirty = ki.build(wl, poison=True)
+    assert torch_isnan_any(dirty.A)
+    a = orc.solve_tril(orc_mod.to_f64(clean.A), clean.cu_seqlens.numpy())
+    b = orc.solve_tril(orc_mod.to_f64(dirty.A), dirty.cu_seqlens.numpy())
+    assert np.array_equal(a, b)
+
+
+def torch_isnan_any(t) -> bool:
+    import torch
+    return bool(torch.isnan(t.float()).any())
+
+
+ALL_CHECKS = [check_golden, check_worked_small, check_rational, check_closed_form,
+              check_exact_64, check_residual, check_layout, check_poison]
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check, oracle_lib):
+    assert oracle_lib.planted() == 0
+    check(oracle_lib)
+
+
+# ------------------------------------------------------- negative controls
+# A copy of the oracle compiled with one deliberate mistake must fail the pins
+# named here; otherwise the pins would not be able to see that mistake.
+PLANTS = {
+    1: ("drops the last term of each row sum", ["check_golden", "check_rational",
+                                                 "check_closed_form", "check_exact_64"]),
+    2: ("wrong sign of the off-diagonal entries", ["check_golden", "check_worked_small",
+                                                    "check_rational", "check_closed_form"]),
+    3: ("packed chunk boundary shifted by one token", ["check_layout"]),
+}
+
+
+@pytest.mark.parametrize("plant", sorted(PLANTS))
+def test_planted_mistake_is_caught(plant, tmp_path):
+    path = orc_mod.compile_oracle(str(tmp_path / f"planted{plant}.so"), plant=plant, openmp=False)
+    bad = orc_mod.Oracle(path)
+    assert bad.planted() == plant
+    _, must_fail = PLANTS[plant]
+    for check in ALL_CHECKS:
+        if check.__name__ in must_fail:
+            with pytest.raises(AssertionError):
+                check(bad)
+
+
+def test_oracle_threads(oracle_lib):
+    assert oracle_lib.num_threads() >= 1
