@@ -1,0 +1,186 @@
+/*
+ * kda_solve_tril.h -- C ABI of the KDA prefill chunk solver for sm_103a.
+ *
+ * Operation (LightLLM PR #1703, "perf(kda): parallelize diagonal solves in
+ * Prefill", PR description): KDA prefill splits every sequence into chunks of
+ * 64 tokens.  For every chunk and every head the solver inverts the unit
+ * lower-triangular matrix (I + A), where A is the chunk's strictly
+ * lower-triangular 64x64 block.  The four independent 16x16 diagonal blocks
+ * are inverted in parallel and then merged into the 64x64 inverse with the
+ * off-diagonal inverse tiles kept in FP32,
+ *
+ *     Linv_ii = (I + A_ii)^-1,
+ *     Linv_ij = -Linv_ii * sum_{k=j}^{i-1} A_ik * Linv_kj      (i > j).
+ *
+ * The same page says the shared solver's 64-token branch "supports both packed
+ * and dense batch layouts" and selects "splitting by the FP32 workspace budget
+ * and minimum input length; the workspace may use at most the FP32 input
+ * size".  The split path runs the diagonal inverses as their own kernel and
+ * keeps the four FP32 16x16 inverse tiles of every chunk-head in a caller
+ * workspace; the single-pass path does everything on chip.  Both paths give
+ * bit-identical results.
+ *
+ * Layouts (all tensors contiguous, row-major, last dimension = 64):
+ *   dense : A, Ai are [B, T, H, 64]; chunks restart at t = 0 of each batch row.
+ *   packed: A, Ai are [1, T, H, 64] with T = cu_seqlens[num_seqs]; request s
+ *           covers rows [cu_seqlens[s], cu_seqlens[s+1]) and its chunks start at
+ *           cu_seqlens[s] + 64 c.  The last chunk of a row or request may hold
+ *           n < 64 rows.
+ * Element (row i, column j) of chunk-head (c, h) is A[t0 + i, h, j] with t0 the
+ * chunk's first row.  Only the strictly lower part of the valid n x n block is
+ * read (j < i < n); the diagonal, the upper triangle and anything at or past
+ * column n may hold any bits, NaN included.  Output rows t0 .. t0+n-1 of Ai
+ * are written in full: the n x n inverse, an exact 1.0 diagonal, exact zeros
+ * above it and exact zeros in columns n .. 63.  No other element of Ai is
+ * touched.
+ *
+ * Ownership: the caller owns every buffer (A, Ai, cu_seqlens, workspace); the
+ * library allocates no device memory and keeps no per-call state.  All device
+ * calls are asynchronous on the given stream (a cudaStream_t passed as void*;
+ * NULL = the legacy default stream) and do not synchronise the host.
+ *
+ * Errors: every function returns a kda_status_t.  Argument errors are found on
+ * the host before any CUDA call and leave all buffers untouched.  KDA_ERR_CUDA
+ * reports a launch failure (cudaGetLastError); faults during asynchronous
+ * execution surface at the caller's next synchronisation, as for any CUDA
+ * kernel.  A kernel whose bounded wait for its own TMA copies runs out (it
+ * never should) stops, and records a code that kda_device_error() returns.
+ */
+#ifndef KDA_SOLVE_TRIL_H
+#define KDA_SOLVE_TRIL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_BT 64                 /* chunk length: the only supported size */
+#define KDA_WS_TILE_BYTES 4096    /* FP32 workspace per chunk-head: 4 tiles of 16x16 */
+
+typedef enum {
+    KDA_F32 = 0,
+    KDA_BF16 = 1,
+    KDA_F16 = 2
+} kda_dtype_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* bad pointer, size, alignment, overlap or layout */
+    KDA_ERR_UNSUPPORTED = 2,      /* dtype or size this build does not handle */
+    KDA_ERR_WORKSPACE = 3,        /* split path forced with a missing or too small workspace */
+    KDA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    KDA_ERR_DEVICE = 5            /* kda_device_error() found a recorded device-side error */
+} kda_status_t;
+
+typedef enum {
+    KDA_PATH_AUTO = 0,            /* let the selector decide (kda_solve_tril_select) */
+    KDA_PATH_SPLIT = 1,           /* diagonal-inverse kernel + merge kernel, FP32 workspace */
+    KDA_PATH_SINGLE = 2           /* one kernel, no workspace */
+} kda_path_t;
+
+/* Smallest T (total rows) for which the selector takes the split path
+ * ("minimum input length", same PR description). */
+#define KDA_SPLIT_MIN_TOKENS 4096
+
+/*
+ * Workspace bytes the split path needs for this shape: KDA_WS_TILE_BYTES per
+ * chunk-head, for an upper bound on the number of chunks that needs no look at
+ * cu_seqlens: B * ceil(T/64) (dense, num_seqs == 0) or min(T, floor((T +
+ * 63 * num_seqs) / 64)) (packed, num_seqs >= 1).  Returns 0 for an empty or
+ * invalid shape.
+ */
+KDA_API size_t kda_solve_tril_workspace_size(int64_t B, int64_t T, int32_t H, int32_t num_seqs);
+
+/*
+ * The path KDA_PATH_AUTO takes for this shape with a workspace of
+ * workspace_bytes (0 = none): KDA_PATH_SPLIT iff the workspace is at least
+ * kda_solve_tril_workspace_size(), that size is at most the FP32 input size
+ * B*T*H*64*4 bytes (equivalently, chunks are on average at least 16 rows full,
+ * "select by chunk occupancy to bound scratch") and B*T >= KDA_SPLIT_MIN_TOKENS;
+ * KDA_PATH_SINGLE otherwise.  Pure host arithmetic.
+ */
+KDA_API kda_path_t kda_solve_tril_select(int64_t B, int64_t T, int32_t H, int32_t num_seqs,
+                                 size_t workspace_bytes);
+
+/*
+ * Solve every chunk-head: Ai = (I + strict_lower(A))^-1 per chunk and head.
+ *
+ *   A           device, [B, T, H, 64] of in_dtype, 16-byte aligned, read only.
+ *   Ai          device, same shape, out_dtype, 16-byte aligned; must not overlap A.
+ *   cu_seqlens  device int32 [num_seqs + 1], or NULL for the dense layout.
+ *               Packed requires B == 1, num_seqs >= 1, cu_seqlens[0] == 0,
+ *               non-decreasing entries and cu_seqlens[num_seqs] == T; the values
+ *               are not read on the host.  Malformed values give unspecified
+ *               results but every access stays inside rows [0, T).
+ *   num_seqs    number of requests (packed) or 0 (dense).
+ *   B, T, H     shape; T == 0 or B == 0 is a no-op returning KDA_OK.  H >= 1,
+ *               B*T < 2^31 and (chunks * H) < 2^31.
+ *   in_dtype    KDA_F32 / KDA_BF16 / KDA_F16; values are widened to FP32.
+ *   out_dtype   KDA_F32 / KDA_BF16 / KDA_F16; FP32 results rounded to nearest even.
+ *   workspace   device, 16-byte aligned, or NULL; used only by the split path.
+ *   workspace_bytes  its size.
+ *   stream      cudaStream_t to launch on.
+ *
+ * Computes in FP32 (FFMA); result within 2e-5*(1+|ref|) of the exact inverse
+ * of the FP32-widened input on the specified workloads.
+ */
+KDA_API kda_status_t kda_solve_tril(const void *A, void *Ai, const int32_t *cu_seqlens,
+                            int32_t num_seqs, int64_t B, int64_t T, int32_t H,
+                            int32_t in_dtype, int32_t out_dtype, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * kda_solve_tril with the path forced.  path = KDA_PATH_AUTO behaves exactly
+ * like kda_solve_tril; KDA_PATH_SPLIT returns KDA_ERR_WORKSPACE when the
+ * workspace is NULL or smaller than kda_solve_tril_workspace_size();
+ * KDA_PATH_SINGLE ignores the workspace.  *path_taken (if not NULL) receives
+ * the path that ran (KDA_PATH_SPLIT or KDA_PATH_SINGLE).
+ */
+KDA_API kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *cu_seqlens,
+                               int32_t num_seqs, int64_t B, int64_t T, int32_t H,
+                               int32_t in_dtype, int32_t out_dtype, void *workspace,
+                               size_t workspace_bytes, void *stream, int32_t path,
+                               int32_t *path_taken);
+
+/*
+ * End-to-end call for callers whose data lives in host memory: copies A (and
+ * cu_seqlens) from host to the caller's device buffers, solves, and copies Ai
+ * back, all enqueued on the stream; the caller synchronises the stream before
+ * reading Ai_host.  Host buffers should be pinned (page-locked) for the copies
+ * to be asynchronous.  A_dev / Ai_dev / cu_dev / workspace follow the rules of
+ * kda_solve_tril; cu_seqlens_host and cu_dev are both NULL for the dense
+ * layout.  Nothing is allocated.
+ */
+KDA_API kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, const int32_t *cu_seqlens_host,
+                                 int32_t num_seqs, int64_t B, int64_t T, int32_t H,
+                                 int32_t in_dtype, int32_t out_dtype, void *A_dev, void *Ai_dev,
+                                 int32_t *cu_dev, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/* Static description of a status code (never NULL). */
+KDA_API const char *kda_status_string(int32_t status);
+
+/*
+ * Read and clear the device-side error word of `device` (synchronises that
+ * device).  *code receives 0 when no kernel of this library recorded an
+ * error since the last call, else a bit set (1 = a bounded TMA wait ran out).
+ * Returns KDA_OK, or KDA_ERR_CUDA when the device cannot be queried.
+ */
+KDA_API kda_status_t kda_device_error(int32_t device, uint32_t *code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+KDA_API int32_t kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_SOLVE_TRIL_H */

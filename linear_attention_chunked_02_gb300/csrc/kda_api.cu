@@ -1,0 +1,270 @@
+// kda_api.cu -- C ABI of the KDA prefill chunk solver: argument checks, the
+// split / single-pass selector, TMA descriptors and kernel dispatch.
+//
+// The selector follows LightLLM PR #1703 (PR description): splitting is chosen
+// "by the FP32 workspace budget and minimum input length; the workspace may
+// use at most the FP32 input size", and the PR summary's "select by chunk
+// occupancy to bound scratch" -- the workspace is 4 KiB per chunk-head and the
+// FP32 input is 256 B per row and head, so the budget holds exactly when
+// chunks are on average at least 16 rows full.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kda_launch.cuh"
+#include "kda_solve_tril.h"
+
+namespace {
+
+__device__ unsigned g_kda_err;   // device-side error word, one per device
+
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1 - 2 * kda::BT;
+
+int elt_size(int32_t dt) { return dt == KDA_F32 ? 4 : 2; }
+bool dtype_ok(int32_t dt) { return dt == KDA_F32 || dt == KDA_BF16 || dt == KDA_F16; }
+
+// Upper bound on the number of chunks that needs no look at cu_seqlens.
+int64_t max_chunks(int64_t B, int64_t T, int32_t num_seqs) {
+    if (B <= 0 || T <= 0) return 0;
+    if (num_seqs <= 0) return B * ((T + kda::BT - 1) / kda::BT);
+    const int64_t bound = (T + int64_t(kda::BT - 1) * num_seqs) / kda::BT;
+    return bound < T ? bound : T;
+}
+
+struct DeviceInfo {
+    int num_sms = 0;
+    unsigned *err = nullptr;
+};
+
+cudaError_t device_info(int device, DeviceInfo &out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[device].num_sms == 0) {
+        int sms = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+        if (e != cudaSuccess) return e;
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_kda_err);
+        if (e != cudaSuccess) return e;
+        cache[device].err = static_cast<unsigned *>(ptr);
+        cache[device].num_sms = sms;
+    }
+    out = cache[device];
+    return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A viewed as a 3-D tensor {64 columns, H heads, rows}; box {16w, 1, 16}.
+bool make_maps(const void *A, int32_t dt, int32_t H, int64_t rows, kda::Maps &maps) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const CUtensorMapDataType ty = dt == KDA_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dt == KDA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t es = cuuint64_t(elt_size(dt));
+    const cuuint64_t dims[3] = {cuuint64_t(kda::BT), cuuint64_t(H), cuuint64_t(rows)};
+    const cuuint64_t strides[2] = {kda::BT * es, cuuint64_t(H) * kda::BT * es};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    for (int w = 0; w < 4; ++w) {
+        const cuuint32_t box[3] = {cuuint32_t(16 * (w + 1)), 1, 16};
+        CUresult r = fn(&maps.m[w], ty, 3, const_cast<void *>(A), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return false;
+    }
+    return true;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaError_t dispatch(int mode, int32_t in_dt, int32_t out_dt, const kda::Maps &maps, const kda::Params &p,
+                     int device, int sms, cudaStream_t s) {
+    switch (in_dt) {
+        case KDA_F32: return kda::launch_f32(mode, out_dt, maps, p, device, sms, s);
+        case KDA_BF16: return kda::launch_bf16(mode, out_dt, maps, p, device, sms, s);
+        default: return kda::launch_f16(mode, out_dt, maps, p, device, sms, s);
+    }
+}
+
+// Host-side checks shared by every entry point.  Returns KDA_OK or an error.
+kda_status_t check_args(const void *A, const void *Ai, const int32_t *cu, int32_t num_seqs, int64_t B,
+                        int64_t T, int32_t H, int32_t in_dt, int32_t out_dt) {
+    if (!dtype_ok(in_dt) || !dtype_ok(out_dt)) return KDA_ERR_UNSUPPORTED;
+    if (H < 1 || B < 0 || T < 0 || num_seqs < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if ((cu != nullptr) != (num_seqs > 0)) return KDA_ERR_INVALID_ARGUMENT;
+    if (cu != nullptr && B != 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (B == 0 || T == 0) return KDA_OK;
+    if (A == nullptr || Ai == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+    if (T > kMaxRows || B > kMaxRows / T) return KDA_ERR_UNSUPPORTED;
+    if (max_chunks(B, T, num_seqs) * H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_solve_tril_workspace_size(int64_t B, int64_t T, int32_t H, int32_t num_seqs) {
+    if (H < 1 || num_seqs < 0) return 0;
+    if (num_seqs > 0 && B != 1) return 0;
+    const int64_t nc = max_chunks(B, T, num_seqs);
+    return size_t(nc) * size_t(H) * KDA_WS_TILE_BYTES;
+}
+
+kda_path_t kda_solve_tril_select(int64_t B, int64_t T, int32_t H, int32_t num_seqs, size_t workspace_bytes) {
+    const size_t need = kda_solve_tril_workspace_size(B, T, H, num_seqs);
+    if (need == 0 || workspace_bytes < need) return KDA_PATH_SINGLE;
+    const size_t fp32_input = size_t(B) * size_t(T) * size_t(H) * kda::BT * 4;
+    if (need > fp32_input) return KDA_PATH_SINGLE;
+    if (B * T < KDA_SPLIT_MIN_TOKENS) return KDA_PATH_SINGLE;
+    return KDA_PATH_SPLIT;
+}
+
+kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B,
+                               int64_t T, int32_t H, int32_t in_dtype, int32_t out_dtype, void *workspace,
+                               size_t workspace_bytes, void *stream, int32_t path, int32_t *path_taken) {
+    if (path != KDA_PATH_AUTO && path != KDA_PATH_SPLIT && path != KDA_PATH_SINGLE)
+        return KDA_ERR_INVALID_ARGUMENT;
+    kda_status_t st = check_args(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype);
+    if (st != KDA_OK) return st;
+    const size_t need = kda_solve_tril_workspace_size(B, T, H, num_seqs);
+    const size_t have = workspace != nullptr ? workspace_bytes : 0;
+    int32_t taken = KDA_PATH_SINGLE;
+    if (path == KDA_PATH_SPLIT) {
+        if (need > 0 && have < need) return KDA_ERR_WORKSPACE;
+        taken = KDA_PATH_SPLIT;
+    } else if (path == KDA_PATH_AUTO) {
+        taken = kda_solve_tril_select(B, T, H, num_seqs, have);
+    }
+    if (path_taken != nullptr) *path_taken = taken;
+    if (B == 0 || T == 0) return KDA_OK;
+    const size_t elems = size_t(B) * size_t(T) * size_t(H) * kda::BT;
+    if (!aligned16(A) || !aligned16(Ai)) return KDA_ERR_INVALID_ARGUMENT;
+    if (overlaps(A, elems * elt_size(in_dtype), Ai, elems * elt_size(out_dtype))) return KDA_ERR_INVALID_ARGUMENT;
+    if (taken == KDA_PATH_SPLIT) {
+        if (!aligned16(workspace)) return KDA_ERR_INVALID_ARGUMENT;
+        if (overlaps(workspace, need, A, elems * elt_size(in_dtype)) ||
+            overlaps(workspace, need, Ai, elems * elt_size(out_dtype)))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+    DeviceInfo info;
+    if (device_info(device, info) != cudaSuccess) return KDA_ERR_CUDA;
+
+    kda::Maps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const int64_t rows = B * T;
+    if (!make_maps(A, in_dtype, H, rows, maps)) return KDA_ERR_CUDA;
+
+    kda::Params p;
+    p.out = Ai;
+    p.ws = static_cast<float *>(workspace);
+    p.cu = cu_seqlens;
+    p.nseq = num_seqs;
+    p.H = H;
+    p.T = T;
+    p.rows = rows;
+    p.cpr = static_cast<int32_t>((T + kda::BT - 1) / kda::BT);
+    p.n_tasks = static_cast<int32_t>(max_chunks(B, T, num_seqs) * H);
+    p.err = info.err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    cudaError_t e;
+    if (taken == KDA_PATH_SPLIT) {
+        e = dispatch(kda::MODE_DIAG, in_dtype, out_dtype, maps, p, device, info.num_sms, s);
+        if (e == cudaSuccess) e = dispatch(kda::MODE_MERGE, in_dtype, out_dtype, maps, p, device, info.num_sms, s);
+    } else {
+        e = dispatch(kda::MODE_FUSED, in_dtype, out_dtype, maps, p, device, info.num_sms, s);
+    }
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_solve_tril(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B,
+                            int64_t T, int32_t H, int32_t in_dtype, int32_t out_dtype, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    return kda_solve_tril_ex(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype, workspace,
+                             workspace_bytes, stream, KDA_PATH_AUTO, nullptr);
+}
+
+kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, const int32_t *cu_seqlens_host,
+                                 int32_t num_seqs, int64_t B, int64_t T, int32_t H, int32_t in_dtype,
+                                 int32_t out_dtype, void *A_dev, void *Ai_dev, int32_t *cu_dev, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+    if ((cu_seqlens_host == nullptr) != (cu_dev == nullptr)) return KDA_ERR_INVALID_ARGUMENT;
+    kda_status_t st = check_args(A_dev, Ai_dev, cu_dev, num_seqs, B, T, H, in_dtype, out_dtype);
+    if (st != KDA_OK) return st;
+    if (B == 0 || T == 0) return KDA_OK;
+    if (A_host == nullptr || Ai_host == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t elems = size_t(B) * size_t(T) * size_t(H) * kda::BT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(A_dev, A_host, elems * elt_size(in_dtype), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cu_dev != nullptr &&
+        cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * size_t(num_seqs + 1), cudaMemcpyHostToDevice,
+                        s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    st = kda_solve_tril(A_dev, Ai_dev, cu_dev, num_seqs, B, T, H, in_dtype, out_dtype, workspace, workspace_bytes,
+                        stream);
+    if (st != KDA_OK) return st;
+    if (cudaMemcpyAsync(Ai_host, Ai_dev, elems * elt_size(out_dtype), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+const char *kda_status_string(int32_t status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported dtype or size";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small for the split path";
+        case KDA_ERR_CUDA: return "CUDA runtime error";
+        case KDA_ERR_DEVICE: return "device-side error recorded";
+        default: return "unknown status";
+    }
+}
+
+kda_status_t kda_device_error(int32_t device, uint32_t *code) {
+    if (code == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaSetDevice(device) != cudaSuccess) return KDA_ERR_CUDA;
+    unsigned v = 0;
+    const unsigned zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_kda_err, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_kda_err, &zero, sizeof(zero));
+    cudaSetDevice(prev);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    *code = v;
+    return KDA_OK;
+}
+
+int32_t kda_version(void) { return 100; }
+
+}  // extern "C"

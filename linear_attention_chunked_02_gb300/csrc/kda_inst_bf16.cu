@@ -1,0 +1,9 @@
+// Kernel instantiations for bf16 input.
+#include "kda_launch.cuh"
+
+namespace kda {
+cudaError_t launch_bf16(int mode, int out_dtype, const Maps &maps, const Params &p, int device, int num_sms,
+                       cudaStream_t stream) {
+    return launch_in<__nv_bfloat16>(mode, out_dtype, maps, p, device, num_sms, stream);
+}
+}  // namespace kda

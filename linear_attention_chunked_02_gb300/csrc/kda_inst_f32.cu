@@ -1,0 +1,9 @@
+// Kernel instantiations for f32 input.
+#include "kda_launch.cuh"
+
+namespace kda {
+cudaError_t launch_f32(int mode, int out_dtype, const Maps &maps, const Params &p, int device, int num_sms,
+                       cudaStream_t stream) {
+    return launch_in<float>(mode, out_dtype, maps, p, device, num_sms, stream);
+}
+}  // namespace kda

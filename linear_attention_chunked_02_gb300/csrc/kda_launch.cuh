@@ -1,0 +1,74 @@
+// kda_launch.cuh -- host-side launch of one kernel instantiation.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kda_kernels.cuh"
+
+namespace kda {
+
+// Per-device cache: opt-in shared memory set and occupancy queried once.
+template <int MODE, typename TIn, typename TOut>
+struct KernelInfo {
+    static int blocks_per_sm(int device, cudaError_t &err) {
+        static std::mutex mu;
+        static int cached[64] = {0};
+        std::lock_guard<std::mutex> lock(mu);
+        err = cudaSuccess;
+        if (device < 0 || device >= 64) {
+            err = cudaErrorInvalidDevice;
+            return 0;
+        }
+        if (cached[device] > 0) return cached[device];
+        auto fn = kda_tril_kernel<MODE, TIn, TOut>;
+        const int bytes = Layout<MODE, TIn>::BYTES;
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (err != cudaSuccess) return 0;
+        int occ = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, NTHREADS, bytes);
+        if (err != cudaSuccess) return 0;
+        cached[device] = occ > 0 ? occ : 1;
+        return cached[device];
+    }
+};
+
+template <int MODE, typename TIn, typename TOut>
+cudaError_t launch_one(const Maps &maps, const Params &p, int device, int num_sms, cudaStream_t stream) {
+    cudaError_t err;
+    const int occ = KernelInfo<MODE, TIn, TOut>::blocks_per_sm(device, err);
+    if (err != cudaSuccess) return err;
+    long long grid = (long long)num_sms * occ;
+    if (grid > p.n_tasks) grid = p.n_tasks;
+    if (grid < 1) return cudaSuccess;
+    kda_tril_kernel<MODE, TIn, TOut>
+        <<<(unsigned)grid, NTHREADS, Layout<MODE, TIn>::BYTES, stream>>>(maps, p);
+    return cudaGetLastError();
+}
+
+// Dispatch on the output dtype (0 f32, 1 bf16, 2 f16) for one input dtype.
+template <typename TIn>
+cudaError_t launch_in(int mode, int out_dtype, const Maps &maps, const Params &p, int device, int num_sms,
+                      cudaStream_t stream) {
+    if (mode == MODE_DIAG) return launch_one<MODE_DIAG, TIn, float>(maps, p, device, num_sms, stream);
+    if (mode == MODE_FUSED) {
+        switch (out_dtype) {
+            case 0: return launch_one<MODE_FUSED, TIn, float>(maps, p, device, num_sms, stream);
+            case 1: return launch_one<MODE_FUSED, TIn, __nv_bfloat16>(maps, p, device, num_sms, stream);
+            default: return launch_one<MODE_FUSED, TIn, __half>(maps, p, device, num_sms, stream);
+        }
+    }
+    switch (out_dtype) {
+        case 0: return launch_one<MODE_MERGE, TIn, float>(maps, p, device, num_sms, stream);
+        case 1: return launch_one<MODE_MERGE, TIn, __nv_bfloat16>(maps, p, device, num_sms, stream);
+        default: return launch_one<MODE_MERGE, TIn, __half>(maps, p, device, num_sms, stream);
+    }
+}
+
+// defined in kda_inst_{f32,bf16,f16}.cu
+cudaError_t launch_f32(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
+cudaError_t launch_bf16(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
+cudaError_t launch_f16(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
+
+}  // namespace kda

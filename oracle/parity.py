@@ -1,0 +1,78 @@
+"""Parity criteria between the CUDA path and the fp64 oracle -- TEST INFRASTRUCTURE.
+
+Tolerances (stated for this solver): against the exact inverse of the rounded
+input, max |got - ref| <= tol * (1 + |ref|) with tol = 2e-5 for fp32 input and
+1e-3 for bf16/fp16 input.  When the output itself is bf16/fp16 the reference
+is first rounded to that dtype and one unit in its last place is added to the
+bound (a correctly rounded bf16 value in [0.5, 1) can sit 2^-9 from the exact
+value, more than 1e-3 * 1.5).  Structural entries -- the unit diagonal, the
+zero upper triangle and the zero columns past a partial chunk's length -- must
+be exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+TOL_IN = {torch.float32: 2e-5, torch.bfloat16: 1e-3, torch.float16: 1e-3}
+MANT_BITS = {torch.bfloat16: 7, torch.float16: 10}
+MIN_EXP = {torch.bfloat16: -126, torch.float16: -14}
+
+
+def round_to(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """fp64 -> fp32 -> dtype, round to nearest even at each step, back to fp64."""
+    return torch.from_numpy(ref.astype(np.float32)).to(dtype).to(torch.float64).numpy()
+
+
+def ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """Spacing of `dtype` numbers at |x| (subnormal spacing near zero)."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.maximum(ax, np.finfo(np.float64).tiny)))
+    e = np.maximum(e, MIN_EXP[dtype])
+    return np.ldexp(1.0, (e - MANT_BITS[dtype]).astype(np.int64))
+
+
+def bound(ref: np.ndarray, in_dtype: torch.dtype, out_dtype: torch.dtype):
+    """(reference to compare with, elementwise allowed |difference|)."""
+    tol = TOL_IN[in_dtype] * (1.0 + np.abs(ref))
+    if out_dtype == torch.float32:
+        return ref, tol
+    return round_to(ref, out_dtype), tol + ulp(ref, out_dtype)
+
+
+def structure_mask(n: int) -> np.ndarray:
+    """[n, 64] True where the output is structurally fixed (diagonal, j > i, j >= n)."""
+    i = np.arange(n)[:, None]
+    j = np.arange(64)[None, :]
+    return j >= i
+
+
+def check_tile(got: np.ndarray, ref: np.ndarray, n: int, in_dtype, out_dtype):
+    """got, ref: [n, 64] of one chunk-head.  Returns (ok, max_excess, where)."""
+    want, tol = bound(ref, in_dtype, out_dtype)
+    st = structure_mask(n)
+    if not np.array_equal(got[st], ref[st]):
+        return False, float("inf"), "structure"
+    diff = np.abs(got - want)
+    excess = diff - tol
+    worst = float(np.max(excess)) if excess.size else -1.0
+    if not np.all(np.isfinite(got)):
+        return False, float("inf"), "non-finite"
+    return worst <= 0.0, worst, "value"
+
+
+def residual(M: np.ndarray, X: np.ndarray) -> float:
+    """||(I + strict_lower(M)) X - I||_max for one n x n chunk."""
+    n = X.shape[0]
+    L = np.eye(n) + np.tril(M[:n, :n], -1)
+    return float(np.abs(L @ X - np.eye(n)).max()) if n else 0.0
+
+
+def residual_bound(M: np.ndarray, X: np.ndarray, out_dtype: torch.dtype) -> float:
+    """1e-4 for fp32/fp16 output; bf16 output adds ||I + M||_inf * 2^-9 * ||X||_max
+    (the exact inverse rounded to bf16 already exceeds 1e-4 on KDA inputs)."""
+    if out_dtype != torch.bfloat16:
+        return 1e-4
+    n = X.shape[0]
+    L = np.eye(n) + np.tril(M[:n, :n], -1)
+    return 1e-4 + float(np.abs(L).sum(1).max()) * 2.0 ** -9 * float(np.abs(X).max())

@@ -1,0 +1,114 @@
+"""The C ABI on a machine without a GPU: loading, exports, sizing, selection and
+argument checks (all of which return before any CUDA call)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import linear_attention_chunked_02_gb300 as kda
+from linear_attention_chunked_02_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return kda.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"kda_solve_tril", "kda_solve_tril_ex", "kda_solve_tril_workspace_size",
+            "kda_solve_tril_select", "kda_solve_tril_host", "kda_status_string",
+            "kda_device_error", "kda_version"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+    bound = {s[0] for s in kda._lib.SIGNATURES}
+    assert names == bound, names ^ bound
+
+
+def test_workspace_size_and_selector(L):
+    # 4 KiB per chunk-head; packed bound min(T, (T + 63 N) / 64)
+    assert kda.workspace_size(1, 8192, 64, 16) == ((8192 + 63 * 16) // 64) * 64 * 4096
+    assert kda.workspace_size(2, 100, 3, 0) == 2 * 2 * 3 * 4096
+    assert kda.workspace_size(1, 5, 1, 5) == 5 * 4096          # capped by T
+    assert kda.workspace_size(0, 0, 1, 0) == 0
+    assert kda.workspace_size(2, 64, 1, 3) == 0                # packed needs B == 1
+    need = kda.workspace_size(1, 8192, 64, 16)
+    assert kda.select_path(1, 8192, 64, 16, need) == "split"
+    assert kda.select_path(1, 8192, 64, 16, need - 1) == "single"
+    assert kda.select_path(1, 8192, 64, 16, 0) == "single"
+    assert kda.select_path(1, 64, 64, 0, 1 << 30) == "single"  # below the minimum length
+    # occupancy < 16 rows per chunk: the workspace would exceed the FP32 input
+    T, N = 8192, 4096                                          # requests of 2 rows
+    assert kda.select_path(1, T, 8, N, 1 << 40) == "single"
+    # the bound counts a possibly partial chunk per request, so 16-row requests
+    # (632 chunks bounded vs 512 real) already exceed it; 32-row requests do not
+    T, N = 8192, 512
+    assert kda.select_path(1, T, 8, N, 1 << 40) == "single"
+    T, N = 8192, 256
+    assert kda.select_path(1, T, 8, N, 1 << 40) == "split"
+
+
+def call(L, A=16, Ai=1 << 20, cu=None, nseq=0, B=1, T=64, H=1, ind=0, outd=0, ws=None, wsb=0, path=0):
+    taken = ctypes.c_int32(-1)
+    st = L.kda_solve_tril_ex(A, Ai, cu, nseq, B, T, H, ind, outd, ws, wsb, None, path, ctypes.byref(taken))
+    return st, taken.value
+
+
+def test_argument_errors_before_any_cuda_call(L):
+    assert call(L, ind=7)[0] == UNSUPPORTED
+    assert call(L, outd=-1)[0] == UNSUPPORTED
+    assert call(L, H=0)[0] == INVALID
+    assert call(L, T=-1)[0] == INVALID
+    assert call(L, cu=4096, nseq=0)[0] == INVALID              # cu_seqlens without a count
+    assert call(L, cu=None, nseq=2)[0] == INVALID
+    assert call(L, cu=4096, nseq=1, B=2)[0] == INVALID         # packed needs B == 1
+    assert call(L, A=None)[0] == INVALID
+    assert call(L, A=8)[0] == INVALID                          # misaligned
+    assert call(L, A=1 << 20, Ai=(1 << 20) + 4096)[0] == INVALID   # overlapping
+    assert call(L, path=5)[0] == INVALID
+    assert call(L, T=1 << 31)[0] == UNSUPPORTED
+    assert call(L, path=1, ws=None)[0] == WORKSPACE            # forced split, no workspace
+    assert call(L, path=1, ws=1 << 24, wsb=100)[0] == WORKSPACE
+    assert call(L, path=1, ws=(1 << 24) + 8, wsb=1 << 20)[0] == INVALID  # misaligned workspace
+    st, taken = call(L, T=0)
+    assert st == OK                                            # empty input is a no-op
+    st, taken = call(L, B=0)
+    assert st == OK
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert L.kda_status_string(s)
+    assert L.kda_status_string(99) == b"unknown status"
+    assert L.kda_version() >= 100
+
+
+def test_no_gpu_reports_cuda_error(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, taken = call(L, A=1 << 20, Ai=1 << 24)
+    assert st == CUDA
+    assert taken == 2
+
+
+def test_host_entry_checks(L):
+    st = L.kda_solve_tril_host(None, None, None, 0, 1, 64, 1, 0, 0, 16, 1 << 20, None, None, 0, None)
+    assert st == INVALID
+    st = L.kda_solve_tril_host(16, 32, 48, 1, 1, 64, 1, 0, 0, 16, 1 << 20, None, None, 0, None)
+    assert st == INVALID                                       # host cu without device cu

@@ -1,0 +1,379 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Axes (LightLLM PR #1703 lists "packed layouts, dtypes, precision modes and
+fallback behavior" as its regression axes): layout {dense, packed} x input
+dtype x output dtype x path {auto, split, single}, shape edges, the specified
+workloads at full size, exact structures, NaN poisoning of ignored elements,
+guard-band canaries, and bitwise equalities between paths and layouts.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as ki
+import oracle
+import oracle.parity as parity
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16, F16 = torch.float32, torch.bfloat16, torch.float16
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from linear_attention_chunked_02_gb300 import build as kbuild
+    kbuild.build()
+    import linear_attention_chunked_02_gb300 as k
+    return k
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+DEV = "cuda:0"
+
+
+def to_dev(inp):
+    A = inp.A.to(DEV)
+    cu = inp.cu_seqlens.to(DEV) if inp.cu_seqlens is not None else None
+    return A, cu
+
+
+def row_geometry(inp):
+    """Per flattened row: (row index inside its chunk, chunk length); -1 for rows in no chunk."""
+    rows = inp.B * inp.T
+    i_in = np.full(rows, -1, dtype=np.int64)
+    n_of = np.zeros(rows, dtype=np.int64)
+    for row0, n in inp.chunks():
+        i_in[row0:row0 + n] = np.arange(n)
+        n_of[row0:row0 + n] = n
+    return i_in, n_of
+
+
+def check_full(inp, got_t, ref, out_dtype, label=""):
+    """Vectorised comparison of every output element against the oracle."""
+    H = inp.H
+    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, 64)
+    ref = ref.reshape(-1, H, 64)
+    i_in, _ = row_geometry(inp)
+    covered = i_in >= 0
+    got, ref, i_in = got[covered], ref[covered], i_in[covered]
+    struct = np.arange(64)[None, None, :] >= i_in[:, None, None]
+    struct = np.broadcast_to(struct, got.shape)
+    assert np.array_equal(got[struct], ref[struct]), f"{label}: structural entries differ"
+    assert np.all(np.isfinite(got)), f"{label}: non-finite output"
+    want, tol = parity.bound(ref, inp.A.dtype, out_dtype)
+    excess = np.abs(got - want) - tol
+    k = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= 0, (f"{label}: max excess {excess.max():.3g} at {k}: got {got[k]!r} "
+                               f"ref {ref[k]!r}")
+
+
+def check_residuals(inp, got_t, out_dtype, limit=2048, seed=0):
+    """||(I + M) X - I||_max per chunk-head on up to `limit` sampled chunk-heads."""
+    H = inp.H
+    A = oracle.to_f64(inp.A).reshape(-1, H, 64)
+    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, 64)
+    tasks = [(r, n, h) for (r, n) in inp.chunks() for h in range(H)]
+    rng = np.random.default_rng(seed)
+    if len(tasks) > limit:
+        tasks = [tasks[i] for i in rng.choice(len(tasks), limit, replace=False)]
+    for r, n, h in tasks:
+        M = A[r:r + n, h, :n]
+        X = got[r:r + n, h, :n]
+        assert parity.residual(M, X) <= parity.residual_bound(M, X, out_dtype), (r, n, h)
+
+
+def solve(kda, inp, out_dtype, path):
+    A, cu = to_dev(inp)
+    out, taken = kda.solve_tril(A, cu, out_dtype=out_dtype, path=path, return_path=True)
+    torch.cuda.synchronize()
+    return out, taken
+
+
+def oracle_ref(orc, inp):
+    return orc.solve_tril(oracle.to_f64(inp.A), inp.cu_seqlens.numpy() if inp.cu_seqlens is not None else None)
+
+
+# ------------------------------------------------------------ small shapes
+
+EDGE_T = [1, 15, 16, 17, 31, 33, 48, 63, 64, 65, 127, 128, 130]
+
+
+@pytest.mark.parametrize("T", EDGE_T)
+@pytest.mark.parametrize("H", [1, 3])
+def test_dense_edges(kda, orc, T, H):
+    inp = ki.build(ki.Workload("edge", "dense", H=H, in_dtype="f32", out_dtype="f32", seed=T * 7 + H,
+                               B=2, T=T, kind="gauss"))
+    ref = oracle_ref(orc, inp)
+    outs = {}
+    for path in ("single", "split"):
+        out, taken = solve(kda, inp, F32, path)
+        assert taken == path
+        check_full(inp, out, ref, F32, f"T={T} H={H} {path}")
+        outs[path] = out
+    assert torch.equal(outs["single"], outs["split"])
+
+
+DTYPES = [F32, BF16, F16]
+
+
+@pytest.mark.parametrize("in_dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("out_dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("kind", ["kda", "gauss", "nodecay"])
+def test_dtype_matrix_packed(kda, orc, in_dtype, out_dtype, kind):
+    names = {F32: "f32", BF16: "bf16", F16: "f16"}
+    inp = ki.build(ki.Workload("dt", "packed", H=4, in_dtype=names[in_dtype], out_dtype=names[out_dtype],
+                               seed=17, seqlens=(1, 63, 64, 65, 200, 0, 128, 7), kind=kind))
+    ref = oracle_ref(orc, inp)
+    outs = {}
+    for path in ("single", "split"):
+        out, taken = solve(kda, inp, out_dtype, path)
+        check_full(inp, out, ref, out_dtype, f"{in_dtype}->{out_dtype} {kind} {path}")
+        outs[path] = out
+    assert torch.equal(outs["single"], outs["split"])
+    check_residuals(inp, outs["single"], out_dtype)
+
+
+@pytest.mark.parametrize("lens", [
+    (0, 0, 5, 0),                      # zero-length requests
+    (1,) * 40,                         # all requests one row long
+    (3000,),                           # one long request
+    tuple(range(1, 70)),               # every partial length
+])
+def test_packed_edges(kda, orc, lens):
+    inp = ki.build(ki.Workload("pe", "packed", H=2, in_dtype="bf16", out_dtype="f32", seed=len(lens),
+                               seqlens=lens, kind="gauss"))
+    ref = oracle_ref(orc, inp)
+    for path in ("single", "split", "auto"):
+        out, _ = solve(kda, inp, F32, path)
+        check_full(inp, out, ref, F32, f"{lens[:4]} {path}")
+
+
+# ------------------------------------------------- exact structures (bitwise)
+
+def _exact_inputs():
+    rng = np.random.default_rng(5)
+    cases = {}
+    I = np.eye(64)
+    cases["zero"] = np.zeros((64, 64))
+    cases["ones"] = np.tril(np.ones((64, 64)), -1)
+    cases["bidiag_half"] = np.diag(np.full(63, 0.5), -1)
+    bd = np.zeros((64, 64))
+    for b in range(4):
+        bd[16 * b:16 * b + 16, 16 * b:16 * b + 16] = np.tril(rng.integers(-2, 3, (16, 16)) * 0.25, -1)
+    cases["blockdiag"] = bd
+    for p in range(4):
+        for q in range(p):
+            M = np.zeros((64, 64))
+            M[16 * p:16 * p + 16, 16 * q:16 * q + 16] = rng.integers(-3, 4, (16, 16)) * 0.5
+            cases[f"block{p}{q}"] = M
+    for chain in ([(1, 0), (2, 1)], [(2, 1), (3, 2)], [(1, 0), (2, 1), (3, 2)], [(3, 1), (1, 0)],
+                  [(2, 0), (3, 2)]):
+        M = np.zeros((64, 64))
+        for p, q in chain:
+            M[16 * p:16 * p + 16, 16 * q:16 * q + 16] = (
+                rng.integers(-1, 2, (16, 16)) * 2.0 ** -rng.integers(0, 3, (16, 16)))
+        cases["chain" + "".join(f"{p}{q}" for p, q in chain)] = M
+    del I
+    return cases
+
+
+EXACT = _exact_inputs()
+
+
+@pytest.mark.parametrize("name", sorted(EXACT))
+def test_exact_structures_bitwise(kda, orc, name):
+    M = EXACT[name]
+    A = torch.from_numpy(M.astype(np.float32)).reshape(1, 64, 1, 64).contiguous()
+    inp = ki.SolverInput(ki.Workload("exact", "dense", H=1, in_dtype="f32", out_dtype="f32", seed=0, T=64),
+                         A, None, [64])
+    ref = oracle_ref(orc, inp)[0, :, 0, :]
+    for path in ("single", "split"):
+        out, _ = solve(kda, inp, F32, path)
+        got = out.cpu().numpy()[0, :, 0, :].astype(np.float64)
+        assert np.array_equal(got, ref), (name, path, np.abs(got - ref).max())
+
+
+# ------------------------------------------------------ robustness checks
+
+def test_poisoned_ignored_elements(kda):
+    wl = ki.Workload("poison", "packed", H=3, in_dtype="f32", out_dtype="f32", seed=23,
+                     seqlens=(5, 64, 100, 1, 70))
+    clean, dirty = ki.build(wl), ki.build(wl, poison=True)
+    for path in ("single", "split"):
+        a, _ = solve(kda, clean, F32, path)
+        b, _ = solve(kda, dirty, F32, path)
+        assert torch.equal(a, b), path
+    wl = wl.with_(layout="dense", seqlens=None, B=2, T=77, in_dtype="bf16")
+    clean, dirty = ki.build(wl), ki.build(wl, poison=True)
+    for path in ("single", "split"):
+        a, _ = solve(kda, clean, F32, path)
+        b, _ = solve(kda, dirty, F32, path)
+        assert torch.equal(a, b), path
+
+
+SENTINEL = {F32: 0x7FC0DEAD, BF16: 0x7FDE, F16: 0x7EAD}
+INT_VIEW = {F32: torch.int32, BF16: torch.int16, F16: torch.int16}
+
+
+@pytest.mark.parametrize("out_dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("layout", ["dense", "packed"])
+def test_guard_band_canaries(kda, out_dtype, layout):
+    """Output and workspace between sentinel-filled guard bands: nothing outside is
+    written, everything inside is."""
+    if layout == "dense":
+        wl = ki.Workload("canary", "dense", H=3, in_dtype="f32", out_dtype="f32", seed=3, B=2, T=81)
+    else:
+        wl = ki.Workload("canary", "packed", H=3, in_dtype="f32", out_dtype="f32", seed=3,
+                         seqlens=(7, 64, 90, 0, 1))
+    inp = ki.build(wl)
+    A, cu = to_dev(inp)
+    pad = 4096
+    n = A.numel()
+    iv = INT_VIEW[out_dtype]
+    buf = torch.full((pad + n + pad,), SENTINEL[out_dtype], dtype=iv, device=DEV)
+    out = buf[pad:pad + n].view(out_dtype).view(A.shape)
+    need = kda.workspace_size(inp.B, inp.T, inp.H, 0 if cu is None else cu.numel() - 1)
+    wpad = 4096
+    wbuf = torch.full((wpad + need + wpad,), 0x5A, dtype=torch.uint8, device=DEV)
+    ws = wbuf[wpad:wpad + need]
+    for path in ("single", "split"):
+        buf[pad:pad + n] = SENTINEL[out_dtype]
+        kda.solve_tril(A, cu, out_dtype=out_dtype, path=path, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == SENTINEL[out_dtype]) and torch.all(buf[pad + n:] == SENTINEL[out_dtype])
+        assert not torch.any(buf[pad:pad + n] == SENTINEL[out_dtype]), path
+        assert torch.all(wbuf[:wpad] == 0x5A) and torch.all(wbuf[wpad + need:] == 0x5A)
+
+
+def test_packed_equals_dense_per_request(kda):
+    lens = (5, 64, 130, 1, 77)
+    wl = ki.Workload("pd", "packed", H=4, in_dtype="bf16", out_dtype="f32", seed=8, seqlens=lens)
+    inp = ki.build(wl)
+    out, _ = solve(kda, inp, F32, "single")
+    cu = inp.cu_seqlens.tolist()
+    for s in range(len(lens)):
+        sub = inp.A[:, cu[s]:cu[s + 1]].contiguous()
+        d = ki.SolverInput(wl.with_(layout="dense", T=lens[s]), sub, None, [lens[s]])
+        o, _ = solve(kda, d, F32, "single")
+        assert torch.equal(o[0], out[0, cu[s]:cu[s + 1]]), s
+
+
+def test_deterministic_repeats(kda):
+    inp = ki.build(ki.Workload("det", "packed", H=8, in_dtype="f16", out_dtype="bf16", seed=9,
+                               seqlens=(300, 64, 17, 1000)))
+    a, _ = solve(kda, inp, BF16, "single")
+    for _ in range(3):
+        b, _ = solve(kda, inp, BF16, "single")
+        assert torch.equal(a, b)
+        c, _ = solve(kda, inp, BF16, "split")
+        assert torch.equal(a, c)
+
+
+def test_selector_fallbacks(kda):
+    # many tiny requests: the workspace would exceed the FP32 input -> single pass
+    lens = tuple(int(x) for x in np.random.default_rng(1).integers(1, 9, size=512))
+    inp = ki.build(ki.Workload("tiny", "packed", H=4, in_dtype="bf16", out_dtype="f32", seed=1, seqlens=lens))
+    out, taken = solve(kda, inp, F32, "auto")
+    assert taken == "single"
+    # forced split with a too-small workspace is an error, not a silent fallback
+    A, cu = to_dev(inp)
+    small = torch.empty(4096, dtype=torch.uint8, device=DEV)
+    with pytest.raises(kda.KdaError) as e:
+        kda.solve_tril(A, cu, path="split", workspace=small)
+    assert e.value.status == 3
+    # auto with an insufficient workspace falls back to single pass
+    out2, taken = kda.solve_tril(A, cu, path="auto", workspace=small, return_path=True)
+    torch.cuda.synchronize()
+    assert taken == "single" and torch.equal(out, out2)
+
+
+def test_host_entry_point(kda):
+    inp = ki.build(ki.Workload("host", "packed", H=4, in_dtype="bf16", out_dtype="f32", seed=12,
+                               seqlens=(100, 64, 3)))
+    A, cu = to_dev(inp)
+    ref, _ = solve(kda, inp, F32, "auto")
+    A_host = inp.A.pin_memory()
+    cu_host = inp.cu_seqlens.pin_memory()
+    Ai_host = torch.empty(inp.A.shape, dtype=F32).pin_memory()
+    A_dev = torch.empty_like(A)
+    Ai_dev = torch.empty(inp.A.shape, dtype=F32, device=DEV)
+    cu_dev = torch.empty_like(cu)
+    kda.solve_tril_host(A_host, Ai_host, A_dev, Ai_dev, cu_host, cu_dev)
+    torch.cuda.synchronize()
+    assert torch.equal(Ai_host, ref.cpu())
+
+
+def test_no_device_error_recorded(kda):
+    assert kda.device_error(0) == 0
+
+
+# ------------------------------------------------- the specified workloads
+
+_CACHE = {}
+
+
+def workload_input(name):
+    if name not in _CACHE:
+        _CACHE.clear()
+        _CACHE[name] = ki.build(ki.WORKLOADS[name])
+    return _CACHE[name]
+
+
+EXPECTED_AUTO = {
+    "dense_1x64_h4_f32": "single",
+    "dense_1x64_h64_bf16": "single",
+    "packed_16x512_h64_f32": "split",
+    "packed_ragged37_h32_bf16": "split",
+    "dense_8x16384_h64_f16": "split",
+}
+
+
+@pytest.mark.parametrize("name", list(ki.WORKLOADS))
+def test_specified_workloads(kda, orc, name):
+    inp = workload_input(name)
+    wl = inp.workload
+    out_dtype = ki.torch_dtype(wl.out_dtype)
+    outs = {}
+    for path in ("auto", "single", "split"):
+        out, taken = solve(kda, inp, out_dtype, path)
+        if path == "auto":
+            assert taken == EXPECTED_AUTO[name]
+        outs[path] = out
+    assert torch.equal(outs["single"], outs["split"])
+    assert torch.equal(outs["auto"], outs["single"])
+    got = outs["auto"]
+    H = inp.H
+    ntask = len(inp.chunks()) * H
+    if ntask <= 40000:
+        ref = oracle_ref(orc, inp)
+        check_full(inp, got, ref, out_dtype, name)
+    else:
+        # full size too large for an all-element fp64 reference: every output
+        # element's structure is checked on the device, values on sampled chunk-heads
+        g = got.view(-1, H, 64)
+        chunks = inp.chunks()
+        i_in = torch.tensor(row_geometry(inp)[0], device=DEV)
+        j = torch.arange(64, device=DEV)
+        upper = (j[None, :] > i_in[:, None])[:, None, :].expand_as(g)
+        diag = (j[None, :] == i_in[:, None])[:, None, :].expand_as(g)
+        assert torch.all(g[upper] == 0) and torch.all(g[diag] == 1)
+        rng = np.random.default_rng(99)
+        A64 = inp.A.view(-1, H, 64)
+        gh = g.cpu()
+        for t in rng.choice(ntask, 1024, replace=False):
+            row0, n = chunks[t // H]
+            h = t % H
+            M = oracle.to_f64(A64[row0:row0 + n, h, :])
+            X = orc.invert_chunk(M, n)[:n, :]
+            ok, worst, where = parity.check_tile(oracle.to_f64(gh[row0:row0 + n, h, :]), X, n,
+                                                 inp.A.dtype, out_dtype)
+            assert ok, (name, row0, h, where, worst)
+    check_residuals(inp, got, out_dtype, limit=1024)
