@@ -69,10 +69,13 @@ def residual(M: np.ndarray, X: np.ndarray) -> float:
 
 
 def residual_bound(M: np.ndarray, X: np.ndarray, out_dtype: torch.dtype) -> float:
-    """1e-4 for fp32/fp16 output; bf16 output adds ||I + M||_inf * 2^-9 * ||X||_max
-    (the exact inverse rounded to bf16 already exceeds 1e-4 on KDA inputs)."""
-    if out_dtype != torch.bfloat16:
+    """1e-4 for fp32 output.  A bf16/fp16 output also carries its own rounding:
+    each entry of X is off by up to half an ulp of the output dtype, which moves
+    the residual by up to ||I + M||_inf * max(ulp(X)) / 2 (the exact inverse
+    rounded to bf16 already exceeds 1e-4 on KDA inputs, and fp16 does so on
+    inputs whose inverse has entries of order one)."""
+    if out_dtype == torch.float32:
         return 1e-4
     n = X.shape[0]
     L = np.eye(n) + np.tril(M[:n, :n], -1)
-    return 1e-4 + float(np.abs(L).sum(1).max()) * 2.0 ** -9 * float(np.abs(X).max())
+    return 1e-4 + float(np.abs(L).sum(1).max()) * 0.5 * float(ulp(X, out_dtype).max())
