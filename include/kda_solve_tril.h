@@ -165,6 +165,40 @@ KDA_API kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, cons
                                  int32_t *cu_dev, void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* Size of the workspace built into the library for kda_solve_tril_split_static. */
+#define KDA_STATIC_WS_BYTES (64u << 20)
+
+/*
+ * Split-path solve that allocates nothing and takes no workspace.  The PR has
+ * no counterpart to this entry point.
+ *
+ * It is for callers that cannot allocate device memory where they call the
+ * solver: a plugin inside a host framework that owns all device memory and
+ * gives its plugins no allocation hook, or a serving loop that fixed its memory
+ * at start-up and must not call cudaMalloc / cudaFree later (those calls can
+ * synchronise the device).  The caller still passes A, Ai and cu_seqlens, with
+ * the meaning, layout and rules of kda_solve_tril; the split path's FP32
+ * workspace is a static device array of KDA_STATIC_WS_BYTES (64 MiB) inside the
+ * library, held by every GPU that loads the library until the process exits.
+ *
+ *   - Shapes whose workspace (kda_solve_tril_workspace_size) exceeds
+ *     KDA_STATIC_WS_BYTES are rejected with KDA_ERR_WORKSPACE before any CUDA
+ *     call; 64 MiB holds 16384 chunk-heads, e.g. the 16 x 512-token, 64-head
+ *     packed solve (35.75 MiB).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls whose kernels
+ *     overlap on the GPU -- on different streams or from different host
+ *     threads -- race on it and give wrong results: issue them in order on one
+ *     stream.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+KDA_API kda_status_t kda_solve_tril_split_static(const void *A, void *Ai, const int32_t *cu_seqlens,
+                                                 int32_t num_seqs, int64_t B, int64_t T, int32_t H,
+                                                 int32_t in_dtype, int32_t out_dtype, void *stream);
+
 /* Static description of a status code (never NULL). */
 KDA_API const char *kda_status_string(int32_t status);
 

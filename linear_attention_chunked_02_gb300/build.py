@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkda_solve_tril.so")
 
-SOURCES = ["kda_api.cu", "kda_inst_f32.cu", "kda_inst_bf16.cu", "kda_inst_f16.cu"]
+SOURCES = ["kda_api.cu", "kda_inst_f32.cu", "kda_inst_bf16.cu", "kda_inst_f16.cu", "kda_no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
