@@ -122,7 +122,7 @@ KDA_API kda_path_t kda_solve_tril_select(int64_t B, int64_t T, int32_t H, int32_
  *               results but every access stays inside rows [0, T).
  *   num_seqs    number of requests (packed) or 0 (dense).
  *   B, T, H     shape; T == 0 or B == 0 is a no-op returning KDA_OK.  H >= 1,
- *               B*T < 2^31 and (chunks * H) < 2^31.
+ *               B*T < 2^31 and (chunks * H) < 2^30.
  *   in_dtype    KDA_F32 / KDA_BF16 / KDA_F16; values are widened to FP32.
  *   out_dtype   KDA_F32 / KDA_BF16 / KDA_F16; FP32 results rounded to nearest even.
  *   workspace   device, 16-byte aligned, or NULL; used only by the split path.

@@ -88,7 +88,7 @@ bool make_maps(const void *A, int32_t dt, int32_t H, int64_t rows, kda::Maps &ma
         const cuuint32_t box[3] = {cuuint32_t(16 * (w + 1)), 1, 16};
         CUresult r = fn(&maps.m[w], ty, 3, const_cast<void *>(A), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return false;
     }
     return true;
@@ -120,7 +120,7 @@ kda_status_t check_args(const void *A, const void *Ai, const int32_t *cu, int32_
     if (B == 0 || T == 0) return KDA_OK;
     if (A == nullptr || Ai == nullptr) return KDA_ERR_INVALID_ARGUMENT;
     if (T > kMaxRows || B > kMaxRows / T) return KDA_ERR_UNSUPPORTED;
-    if (max_chunks(B, T, num_seqs) * H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (max_chunks(B, T, num_seqs) * H > INT32_MAX / 2) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
 }
 

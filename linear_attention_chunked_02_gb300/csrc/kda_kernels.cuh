@@ -10,26 +10,32 @@
 //   * One persistent CTA of 64 threads (four 16-lane "units") per resident
 //     slot; a CTA walks its chunk-heads q = blockIdx.x, blockIdx.x + grid, ...
 //     (q = chunk * H + head, so neighbouring CTAs share the chunk's token rows).
-//   * A thread issues TMA tile loads (cp.async.bulk.tensor, mbarrier
-//     completion) for the next chunk-head while the CTA computes the current
-//     one (2-stage ring).  Only the ten lower 16x16 blocks of each chunk are
-//     fetched: block-row r as one box of 16 rows x 16(r+1) columns.
+//   * Thread 0 issues TMA tile loads (cp.async.bulk.tensor, mbarrier
+//     completion) into a 2-stage ring, so the next chunk-head is in flight
+//     while the current one is computed.  Only the ten lower 16x16 blocks are
+//     fetched: block-row r as one box of 16 rows x 16(r+1) columns.  FP32 input
+//     is used in place from the landing buffer; 16-bit input is widened once.
 //   * Diagonal blocks: one unit per block, one lane per column, forward
-//     substitution in registers (fp32 FMA).
+//     substitution in registers (FP32 FMA).
 //   * Merge, as two 32x32 levels (the 64x64 matrix is lower block-triangular
 //     with 32x32 blocks TL, BR and off-diagonal BL):
 //        level A: X10 = -(X11 A10) X00,  X32 = -(X33 A32) X22
 //        level B: U = X_BR A_BL,  X_BL = -U X_TL
-//     which is Linv_ij = -Linv_ii sum_k A_ik Linv_kj regrouped.  Every product
-//     is a 16x16x16 FP32 FMA product computed by one unit with a 4x4 register
-//     tile per lane; products with a triangular factor skip the k-quads whose
-//     factor entries are structurally zero.
-//   * The output tile (n rows x 64 columns incl. exact zeros and the unit
-//     diagonal) is written with 16-byte coalesced stores.
-//   * Split path: MODE_DIAG runs only the diagonal inverses and stores their
-//     FP32 tiles to the workspace; MODE_MERGE loads them back and runs the
-//     merge.  Both call the same device functions as MODE_FUSED, so every
-//     element is computed with the same operations in the same order.
+//     which is Linv_ij = -Linv_ii sum_k A_ik Linv_kj regrouped.  Each 16x16x16
+//     FP32 product is computed by one unit with a 4x4 register tile per lane.
+//     The U blocks are kept negated (U' = -U), so only two product kinds
+//     exist: "lower-triangular left factor, negated" (which skips the k-quads
+//     where the diagonal inverse is structurally zero) and "dense".  The
+//     products run as a 4-step loop over a fixed schedule in which all four
+//     units are busy in every step; one call site per product kind keeps the
+//     code small enough for the instruction cache.
+//   * Every output block is stored straight from the registers that computed
+//     it (16-byte row segments), the zero blocks above the diagonal directly.
+//   * Split path: MODE_DIAG inverts the diagonal blocks, writes them (and the
+//     zero blocks) to the output and their FP32 tiles to the workspace;
+//     MODE_MERGE loads the tiles back and produces the off-diagonal blocks.
+//     Both call the same device functions as MODE_FUSED, so every element is
+//     computed with the same operations in the same order.
 #pragma once
 
 #include <cuda.h>
@@ -48,27 +54,28 @@ constexpr int MODE_FUSED = 0;
 constexpr int MODE_DIAG = 1;
 constexpr int MODE_MERGE = 2;
 
-// FP32 on-chip tiles.  A blocks: pitch 16, block stride 272 floats (1088 B) so
-// that blocks with odd slot distance sit in different bank quads.  X / U
-// blocks: pitch 20 floats (rows 4 apart land in distinct bank quads), block
-// stride 336 floats (1344 B).
-constexpr int AP = 16;
-constexpr int ABS = 272;
+// On-chip FP32 tiles.  X / U blocks: pitch 20 floats (rows 4 apart land in
+// distinct bank quads), block stride 336 floats.  Widened 16-bit A blocks:
+// pitch 16, block stride 272 floats.
 constexpr int XP = 20;
 constexpr int XBS = 336;
+constexpr int AP16 = 16;
+constexpr int ABS = 272;
 
 __host__ __device__ constexpr int blk(int i, int j) { return i * (i + 1) / 2 + j; }
 
-// transposed-copy slots and U slots
-constexpr int T_X00 = 0, T_X22 = 1, T_X11 = 2, T_X10 = 3;
-constexpr int U_00 = 0, U_10 = 1, U_01 = 2, U_11 = 3;
+// X slots 0..3 hold the diagonal inverses X00..X33; slot 4 X10, slot 5 -X32.
+constexpr int XS_10 = 4, XS_32N = 5;
+// Diagonal block inverted by each unit: warp 0 takes X11 and X33, warp 1 X00
+// and X22, so that the first merge step only needs the unit's own warp.
+__host__ __device__ constexpr int diag_of_unit(int u) { return u == 0 ? 1 : u == 1 ? 3 : u == 2 ? 0 : 2; }
 
 // device-side error word (bit 0: a bounded TMA wait ran out)
 constexpr unsigned ERR_WAIT_TIMEOUT = 1u;
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
 
 struct Params {
-    void *out;                 // Ai (MODE_FUSED / MODE_MERGE)
+    void *out;                 // Ai
     float *ws;                 // workspace tiles (MODE_DIAG writes, MODE_MERGE reads)
     const int32_t *cu;         // packed: cu_seqlens (device); dense: nullptr
     int32_t nseq;
@@ -182,7 +189,7 @@ template <> struct Elt<__half> {
     }
 };
 
-// 8 fp32 -> 16 bytes of bf16 / fp16 (round to nearest even)
+// output element conversion (round to nearest even)
 __device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16 *) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -191,40 +198,71 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half *) {
     __half2 v = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+__device__ __forceinline__ void put1(float *p, float v) { *p = v; }
+__device__ __forceinline__ void put1(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void put1(__half *p, float v) { *p = __float2half_rn(v); }
+// four consecutive output elements
+__device__ __forceinline__ void put4(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+template <typename TOut>
+__device__ __forceinline__ void put4(TOut *p, float a, float b, float c, float d) {
+    uint2 o;
+    o.x = pack2(a, b, (TOut *)nullptr);
+    o.y = pack2(c, d, (TOut *)nullptr);
+    *reinterpret_cast<uint2 *>(p) = o;
+}
 
 // ------------------------------------------------------------ smem layout
 template <int MODE, typename TIn>
 struct Layout {
     static constexpr int ELT = sizeof(TIn);
+    static constexpr bool WIDEN = ELT == 2;
     // stage: raw TMA landing area
     static constexpr int A_ELEMS = MODE == MODE_FUSED ? 10 * 256 : MODE == MODE_DIAG ? 4 * 256 : 6 * 256;
     static constexpr int A_BYTES = A_ELEMS * ELT;
     static constexpr int WS_OFF = (A_BYTES + 127) / 128 * 128;
     static constexpr int STAGE_BYTES = MODE == MODE_MERGE ? WS_OFF + 4096 : WS_OFF;
     static constexpr uint32_t TX_BYTES = MODE == MODE_MERGE ? A_BYTES + 4096 : A_BYTES;
-    static constexpr int NAF = MODE == MODE_DIAG ? 4 : 10;     // A-block slots
-    static constexpr int NXN = MODE == MODE_DIAG ? 0 : 10;     // X-block slots
-    static constexpr int NXT = MODE == MODE_DIAG ? 0 : 4;
+    static constexpr int NAF = WIDEN ? (MODE == MODE_DIAG ? 4 : 10) : 0;   // widened A-block slots
+    static constexpr int NX = MODE == MODE_DIAG ? 0 : 6;
     static constexpr int NU = MODE == MODE_DIAG ? 0 : 4;
     static constexpr int OFF_BAR = 0;
     static constexpr int OFF_META = 64;
     static constexpr int OFF_STAGE = 128;
     static constexpr int OFF_AF = OFF_STAGE + STAGES * STAGE_BYTES;
-    static constexpr int OFF_XN = OFF_AF + NAF * ABS * 4;
-    static constexpr int OFF_XT = OFF_XN + NXN * XBS * 4;
-    static constexpr int OFF_U = OFF_XT + NXT * XBS * 4;
+    static constexpr int OFF_X = OFF_AF + NAF * ABS * 4;
+    static constexpr int OFF_U = OFF_X + NX * XBS * 4;
     static constexpr int BYTES = OFF_U + NU * XBS * 4;
-    // stage offset (bytes) of block-row r's box
+    // stage offset (bytes) of block-row r's box, and the box width in elements
     __host__ __device__ static constexpr int row_off(int r) {
         return MODE == MODE_FUSED ? 256 * ELT * (r * (r + 1) / 2)
              : MODE == MODE_DIAG  ? 256 * ELT * r
                                   : 256 * ELT * ((r - 1) * r / 2);
     }
+    __host__ __device__ static constexpr int width(int r) {
+        return MODE == MODE_FUSED ? 16 * (r + 1) : MODE == MODE_DIAG ? 16 : 16 * r;
+    }
+    static constexpr int R0 = MODE == MODE_MERGE ? 1 : 0;   // first block-row fetched
 };
 
-// A-block slot of block (i, j) in the Af area
+// A-block slot of block (i, j) in the widened area
 template <int MODE>
 __device__ __forceinline__ int af_slot(int i, int j) { return MODE == MODE_DIAG ? i : blk(i, j); }
+
+// An FP32 view of A block (i, j): pointer and row pitch (floats).
+struct AView {
+    const float *p;
+    int pitch;
+};
+template <int MODE, typename TIn>
+__device__ __forceinline__ AView aview(const unsigned char *stage, const float *Af, int i, int j) {
+    using L = Layout<MODE, TIn>;
+    if (L::WIDEN) return {Af + af_slot<MODE>(i, j) * ABS, AP16};
+    const float *base = reinterpret_cast<const float *>(stage + L::row_off(i));
+    if (MODE == MODE_DIAG) return {base, 16};
+    return {base + 16 * j, L::width(i)};
+}
 
 // ------------------------------------------------------------ task decode
 // Per-CTA state of the walk over cu_seqlens (packed layout).
@@ -306,9 +344,10 @@ __device__ __forceinline__ void issue(const Params &p, const CUtensorMap *maps, 
     }
 }
 
-// --------------------------------------------------------- stage -> FP32
-// Box of block-row r: 16 rows x (16 * nb) elements starting at block column c0.
-// Rows at or past n become exact zeros (they may hold the next request's data).
+// ------------------------------------------------------ operand preparation
+// 16-bit input: block-row R's box (16 rows x 16*NB elements from block column
+// C0) widened to FP32 tiles; rows at or past n become exact zeros (they may
+// hold the next request's rows).
 template <int MODE, typename TIn, int R, int C0, int NB>
 __device__ __forceinline__ void widen_box(const unsigned char *src, float *Af, int n, int tid) {
     constexpr int VEC = Elt<TIn>::VEC;
@@ -326,7 +365,7 @@ __device__ __forceinline__ void widen_box(const unsigned char *src, float *Af, i
             float f[VEC];
             Elt<TIn>::widen(v, f);
             const bool keep = full || (16 * R + i < n);
-            float *dst = Af + af_slot<MODE>(R, C0 + k / 16) * ABS + i * AP + (k & 15);
+            float *dst = Af + af_slot<MODE>(R, C0 + k / 16) * ABS + i * AP16 + (k & 15);
 #pragma unroll
             for (int t = 0; t < VEC; t += 4) {
                 float4 o;
@@ -340,11 +379,46 @@ __device__ __forceinline__ void widen_box(const unsigned char *src, float *Af, i
     }
 }
 
+template <int MODE, typename TIn>
+__device__ __forceinline__ void widen_all(const unsigned char *stage, float *Af, int n, int tid) {
+    using L = Layout<MODE, TIn>;
+    if (MODE == MODE_FUSED) {
+        widen_box<MODE, TIn, 0, 0, 1>(stage + L::row_off(0), Af, n, tid);
+        widen_box<MODE, TIn, 1, 0, 2>(stage + L::row_off(1), Af, n, tid);
+        widen_box<MODE, TIn, 2, 0, 3>(stage + L::row_off(2), Af, n, tid);
+        widen_box<MODE, TIn, 3, 0, 4>(stage + L::row_off(3), Af, n, tid);
+    } else if (MODE == MODE_DIAG) {
+        widen_box<MODE, TIn, 0, 0, 1>(stage + L::row_off(0), Af, n, tid);
+        widen_box<MODE, TIn, 1, 1, 1>(stage + L::row_off(1), Af, n, tid);
+        widen_box<MODE, TIn, 2, 2, 1>(stage + L::row_off(2), Af, n, tid);
+        widen_box<MODE, TIn, 3, 3, 1>(stage + L::row_off(3), Af, n, tid);
+    } else {
+        widen_box<MODE, TIn, 1, 0, 1>(stage + L::row_off(1), Af, n, tid);
+        widen_box<MODE, TIn, 2, 0, 2>(stage + L::row_off(2), Af, n, tid);
+        widen_box<MODE, TIn, 3, 0, 3>(stage + L::row_off(3), Af, n, tid);
+    }
+}
+
+// FP32 input used in place: zero the rows at or past n of a partial chunk.
+template <int MODE>
+__device__ __forceinline__ void zero_rows(unsigned char *stage, int n, int tid) {
+    using L = Layout<MODE, float>;
+#pragma unroll
+    for (int r = L::R0; r < 4; ++r) {
+        const int w4 = L::width(r) / 4;                       // float4 per row
+        float4 *base = reinterpret_cast<float4 *>(stage + L::row_off(r));
+        for (int e = tid; e < 16 * w4; e += NTHREADS) {
+            const int i = e / w4;
+            if (16 * r + i >= n) base[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
 // ------------------------------------------------------ diagonal inverse
 // Unit-lower-triangular 16x16 inverse by forward substitution, one lane per
-// column j: x[i] = -sum_{k<i} a[i][k] x[k] for i > j, x[j] = 1, x[i<j] = 0.
-// `a` holds the block (pitch AP); only entries with k < i are used.
-__device__ __forceinline__ void diag_invert(const float *a, int j, float (&x)[16]) {
+// column j: x[i] = sum_{k<i} (-a[i][k]) x[k] for i > j, x[j] = 1, x[i<j] = 0.
+// Only entries of `a` (pitch ap) with k < i are used.
+__device__ __forceinline__ void diag_invert(const float *a, int ap, int j, float (&x)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
@@ -352,71 +426,47 @@ __device__ __forceinline__ void diag_invert(const float *a, int j, float (&x)[16
         float s = 0.f;
 #pragma unroll
         for (int kq = 0; kq < (i + 3) / 4; ++kq) {
-            const float4 v = *reinterpret_cast<const float4 *>(a + i * AP + 4 * kq);
-            if (4 * kq + 0 < i) s = fmaf(v.x, x[4 * kq + 0], s);
-            if (4 * kq + 1 < i) s = fmaf(v.y, x[4 * kq + 1], s);
-            if (4 * kq + 2 < i) s = fmaf(v.z, x[4 * kq + 2], s);
-            if (4 * kq + 3 < i) s = fmaf(v.w, x[4 * kq + 3], s);
+            const float4 v = *reinterpret_cast<const float4 *>(a + i * ap + 4 * kq);
+            if (4 * kq + 0 < i) s = fmaf(-v.x, x[4 * kq + 0], s);
+            if (4 * kq + 1 < i) s = fmaf(-v.y, x[4 * kq + 1], s);
+            if (4 * kq + 2 < i) s = fmaf(-v.z, x[4 * kq + 2], s);
+            if (4 * kq + 3 < i) s = fmaf(-v.w, x[4 * kq + 3], s);
         }
-        x[i] = (i > j) ? -s : x[i];
+        x[i] = (i > j) ? s : x[i];
     }
 }
 
 // ----------------------------------------------------------- 16x16 products
 // A unit computes a 16x16 tile; lane l (0..15): rg = l >> 2, cg = l & 3.
-// acc[m][n] is row rg + 4m.  prod_left: column 4cg + n.  prod_right: column cg + 4n.
+// acc[m][n] is row rg + 4m, column 4cg + n.
 
 __device__ __forceinline__ float comp(const float4 &v, int kk) {
     return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
 }
 
-// acc += P Q; P row-major (pitch pp), Q row-major (pitch qp).  LTRI: P is lower
-// triangular, so k-quad q only meets rows m >= q.
-template <bool LTRI>
-__device__ __forceinline__ void prod_left(float (&acc)[4][4], const float *__restrict__ P, int pp,
-                                          const float *__restrict__ Q, int qp, int rg, int cg) {
+// TRI_NEG = false: acc += P Q.  TRI_NEG = true: acc -= P Q with P lower
+// triangular, so k-quad q only meets rows m >= q (the negation is folded into
+// the FMA operand).  P row-major with pitch XP, Q row-major with pitch qp.
+template <bool TRI_NEG>
+__device__ __forceinline__ void prod(float (&acc)[4][4], const float *__restrict__ P,
+                                     const float *__restrict__ Q, int qp, int rg, int cg) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         float4 pr[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-            if (!LTRI || m >= q) pr[m] = *reinterpret_cast<const float4 *>(P + (rg + 4 * m) * pp + 4 * q);
+            if (!TRI_NEG || m >= q) pr[m] = *reinterpret_cast<const float4 *>(P + (rg + 4 * m) * XP + 4 * q);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const float4 qv = *reinterpret_cast<const float4 *>(Q + (4 * q + kk) * qp + 4 * cg);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                if (LTRI && m < q) continue;
-                const float a = comp(pr[m], kk);
+                if (TRI_NEG && m < q) continue;
+                const float a = TRI_NEG ? -comp(pr[m], kk) : comp(pr[m], kk);
                 acc[m][0] = fmaf(a, qv.x, acc[m][0]);
                 acc[m][1] = fmaf(a, qv.y, acc[m][1]);
                 acc[m][2] = fmaf(a, qv.z, acc[m][2]);
                 acc[m][3] = fmaf(a, qv.w, acc[m][3]);
-            }
-        }
-    }
-}
-
-// acc += P R with R given transposed (Rt[c * XP + k] = R[k][c]).  RTRI: R is
-// lower triangular, so column cg + 4n only meets k-quads q >= n.
-template <bool RTRI>
-__device__ __forceinline__ void prod_right(float (&acc)[4][4], const float *__restrict__ P, int pp,
-                                           const float *__restrict__ Rt, int rg, int cg) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        float4 pr[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) pr[m] = *reinterpret_cast<const float4 *>(P + (rg + 4 * m) * pp + 4 * q);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-            if (RTRI && n > q) continue;
-            const float4 rt = *reinterpret_cast<const float4 *>(Rt + (cg + 4 * n) * XP + 4 * q);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                acc[m][n] = fmaf(pr[m].x, rt.x, acc[m][n]);
-                acc[m][n] = fmaf(pr[m].y, rt.y, acc[m][n]);
-                acc[m][n] = fmaf(pr[m].z, rt.z, acc[m][n]);
-                acc[m][n] = fmaf(pr[m].w, rt.w, acc[m][n]);
             }
         }
     }
@@ -429,126 +479,52 @@ __device__ __forceinline__ void zero(float (&acc)[4][4]) {
         for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
 }
 
-// tile from prod_left (columns 4cg + n) -> row-major block
-__device__ __forceinline__ void put_left(float *dst, const float (&acc)[4][4], int rg, int cg) {
+// (+/-) tile -> row-major X/U block
+template <bool NEG>
+__device__ __forceinline__ void put_smem(float *dst, const float (&acc)[4][4], int rg, int cg) {
+    const float s = NEG ? -1.f : 1.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m)
         *reinterpret_cast<float4 *>(dst + (rg + 4 * m) * XP + 4 * cg) =
-            make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-}
-// -tile from prod_right (columns cg + 4n) -> row-major block (+ transposed copy)
-__device__ __forceinline__ void put_right_neg(float *dst, float *dstT, const float (&acc)[4][4], int rg,
-                                              int cg) {
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int n = 0; n < 4; ++n) dst[(rg + 4 * m) * XP + cg + 4 * n] = -acc[m][n];
-    if (dstT != nullptr) {
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) dstT[(cg + 4 * n) * XP + rg + 4 * m] = -acc[m][n];
-    }
+            make_float4(s * acc[m][0], s * acc[m][1], s * acc[m][2], s * acc[m][3]);
 }
 
-// ------------------------------------------------------------------ merge
-// Inputs: Xn diagonal blocks (row-major), Xt transposed X00/X11/X22, Af
-// off-diagonal A blocks.  Outputs: the six off-diagonal X blocks in Xn.
-__device__ __forceinline__ void merge(const float *Af, float *Xn, float *Xt, float *U, int tid) {
-    const int unit = tid >> 4, warp = tid >> 5, half = unit & 1;
-    const int l = tid & 15, rg = l >> 2, cg = l & 3;
-    float acc[4][4];
-    // level A (warp 0): X10 = -(X11 A10) X00 ; X32 = -(X33 A32) X22
-    if (warp == 0) {
-        zero(acc);
-        prod_left<true>(acc, Xn + (half ? blk(3, 3) : blk(1, 1)) * XBS, XP,
-                        Af + (half ? blk(3, 2) : blk(1, 0)) * ABS, AP, rg, cg);
-        put_left(U + half * XBS, acc, rg, cg);
-        __syncwarp();
-        zero(acc);
-        prod_right<true>(acc, U + half * XBS, XP, Xt + (half ? T_X22 : T_X00) * XBS, rg, cg);
-        put_right_neg(Xn + (half ? blk(3, 2) : blk(1, 0)) * XBS, half ? nullptr : Xt + T_X10 * XBS, acc,
-                      rg, cg);
-    }
-    __syncthreads();
-    // level B, step 1: U = X_BR A_BL
-    zero(acc);
-    if (warp == 0) {     // U00 = X22 A20 ; U01 = X22 A21
-        prod_left<true>(acc, Xn + blk(2, 2) * XBS, XP, Af + blk(2, half) * ABS, AP, rg, cg);
-        put_left(U + (half ? U_01 : U_00) * XBS, acc, rg, cg);
-    } else {             // U10 = X32 A20 + X33 A30 ; U11 = X32 A21 + X33 A31
-        prod_left<false>(acc, Xn + blk(3, 2) * XBS, XP, Af + blk(2, half) * ABS, AP, rg, cg);
-        prod_left<true>(acc, Xn + blk(3, 3) * XBS, XP, Af + blk(3, half) * ABS, AP, rg, cg);
-        put_left(U + (half ? U_11 : U_10) * XBS, acc, rg, cg);
-    }
-    __syncthreads();
-    // level B, step 2: X_BL = -U X_TL
-    zero(acc);
-    if (warp == 0) {     // X21 = -U01 X11 ; X31 = -U11 X11
-        prod_right<true>(acc, U + (half ? U_11 : U_01) * XBS, XP, Xt + T_X11 * XBS, rg, cg);
-        put_right_neg(Xn + (half ? blk(3, 1) : blk(2, 1)) * XBS, nullptr, acc, rg, cg);
-    } else {             // X20 = -(U00 X00 + U01 X10) ; X30 = -(U10 X00 + U11 X10)
-        prod_right<true>(acc, U + (half ? U_10 : U_00) * XBS, XP, Xt + T_X00 * XBS, rg, cg);
-        prod_right<false>(acc, U + (half ? U_11 : U_01) * XBS, XP, Xt + T_X10 * XBS, rg, cg);
-        put_right_neg(Xn + (half ? blk(3, 0) : blk(2, 0)) * XBS, nullptr, acc, rg, cg);
-    }
-    __syncthreads();
-}
-
-// ----------------------------------------------------------- output store
+// tile -> output block (bi, bj) of the chunk, rows below n only
 template <typename TOut>
-__device__ __forceinline__ void store_tile(TOut *out, const Meta &m, int H, const float *Xn, int tid);
-
-template <>
-__device__ __forceinline__ void store_tile<float>(float *out, const Meta &m, int H, const float *Xn, int tid) {
-    // 64 rows x 16 float4; thread covers rows (tid >> 4) + 4v, float4 column tid & 15
-    const int c4 = tid & 15, bc = c4 >> 2;
+__device__ __forceinline__ void put_out(TOut *out, const Meta &m, int H, int bi, int bj,
+                                        const float (&acc)[4][4], int rg, int cg) {
 #pragma unroll
-    for (int v = 0; v < 16; ++v) {
-        const int r = (tid >> 4) + 4 * v;
+    for (int mm = 0; mm < 4; ++mm) {
+        const int r = 16 * bi + rg + 4 * mm;
         if (r < m.n) {
-            const int br = r >> 4;
-            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (bc <= br) val = *reinterpret_cast<const float4 *>(Xn + blk(br, bc) * XBS + (r & 15) * XP + 4 * (c4 & 3));
-            float *dst = out + (int64_t(m.row0 + r) * H + m.h) * BT + 4 * c4;
-            *reinterpret_cast<float4 *>(dst) = val;
+            TOut *dst = out + (int64_t(m.row0 + r) * H + m.h) * BT + 16 * bj + 4 * cg;
+            put4(dst, acc[mm][0], acc[mm][1], acc[mm][2], acc[mm][3]);
         }
     }
 }
 
+// The zero blocks above the diagonal (columns 16(br+1) .. 63 of rows in block-row br).
 template <typename TOut>
-__device__ __forceinline__ void store_tile_16(TOut *out, const Meta &m, int H, const float *Xn, int tid) {
-    // 64 rows x 8 groups of 8; thread covers rows (tid >> 3) + 8v, group tid & 7
-    const int c8 = tid & 7, bc = c8 >> 1;
+__device__ __forceinline__ void store_upper_zeros(TOut *out, const Meta &m, int H, int tid) {
+    constexpr int VEC = 16 / int(sizeof(TOut));     // elements per 16-byte store
+    constexpr int PB = 16 / VEC;                    // 16-byte stores per 16-column block
 #pragma unroll
-    for (int v = 0; v < 8; ++v) {
-        const int r = (tid >> 3) + 8 * v;
-        if (r < m.n) {
-            const int br = r >> 4;
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-            if (bc <= br) {
-                const float *src = Xn + blk(br, bc) * XBS + (r & 15) * XP + 8 * (c8 & 1);
-                a = *reinterpret_cast<const float4 *>(src);
-                b = *reinterpret_cast<const float4 *>(src + 4);
+    for (int br = 0; br < 3; ++br) {
+        const int per_row = PB * (3 - br);
+        const int cnt = 16 * per_row;
+#pragma unroll
+        for (int e0 = 0; e0 < cnt; e0 += NTHREADS) {
+            const int e = e0 + tid;
+            if (e < cnt) {
+                const int r = 16 * br + e / per_row;
+                const int c = 16 * (br + 1) + VEC * (e % per_row);
+                if (r < m.n) {
+                    TOut *dst = out + (int64_t(m.row0 + r) * H + m.h) * BT + c;
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
-            uint4 o;
-            o.x = pack2(a.x, a.y, (TOut *)nullptr);
-            o.y = pack2(a.z, a.w, (TOut *)nullptr);
-            o.z = pack2(b.x, b.y, (TOut *)nullptr);
-            o.w = pack2(b.z, b.w, (TOut *)nullptr);
-            TOut *dst = out + (int64_t(m.row0 + r) * H + m.h) * BT + 8 * c8;
-            *reinterpret_cast<uint4 *>(dst) = o;
         }
     }
-}
-template <>
-__device__ __forceinline__ void store_tile<__nv_bfloat16>(__nv_bfloat16 *out, const Meta &m, int H,
-                                                          const float *Xn, int tid) {
-    store_tile_16(out, m, H, Xn, tid);
-}
-template <>
-__device__ __forceinline__ void store_tile<__half>(__half *out, const Meta &m, int H, const float *Xn, int tid) {
-    store_tile_16(out, m, H, Xn, tid);
 }
 
 // ----------------------------------------------------------------- kernel
@@ -564,10 +540,12 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     const Meta *metas = reinterpret_cast<const Meta *>(smem + L::OFF_META);
     float *Af = reinterpret_cast<float *>(smem + L::OFF_AF);
-    float *Xn = reinterpret_cast<float *>(smem + L::OFF_XN);
-    float *Xt = reinterpret_cast<float *>(smem + L::OFF_XT);
+    float *Xs = reinterpret_cast<float *>(smem + L::OFF_X);
     float *U = reinterpret_cast<float *>(smem + L::OFF_U);
+    TOut *out = reinterpret_cast<TOut *>(p.out);
     const int tid = threadIdx.x;
+    const int unit = tid >> 4, warp = tid >> 5, half = unit & 1;
+    const int l = tid & 15, rg = l >> 2, cg = l & 3;
     const int32_t G = gridDim.x;
     Walk walk{0, 0};
 
@@ -585,81 +563,179 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         const uint32_t parity = (it / STAGES) & 1;
         const bool ok = mbar_wait_bounded(&bars[st], parity);
         if (__syncthreads_or(!ok)) {
-            // A copy never completed.  Record it, give the other stage's copy a
-            // bounded chance to land, and stop; nothing else is in flight.
+            // A copy never completed.  Record it, give the copies still in
+            // flight a bounded chance to land, and stop.
             if (tid == 0) {
                 atomicOr(p.err, ERR_WAIT_TIMEOUT);
-                mbar_wait_bounded(&bars[(st + 1) % STAGES], ((it + 1) / STAGES) & 1);
+                mbar_wait_bounded(&bars[st], parity);
+                for (int s = 1; s < STAGES; ++s)
+                    mbar_wait_bounded(&bars[(st + s) % STAGES], ((it + s) / STAGES) & 1);
             }
             return;
         }
         const Meta m = metas[st];
         if (!m.valid) break;
-        const unsigned char *stage = smem + L::OFF_STAGE + st * L::STAGE_BYTES;
+        unsigned char *stage = smem + L::OFF_STAGE + st * L::STAGE_BYTES;
         const int32_t q = int32_t(blockIdx.x) + it * G;
+        const int32_t q_next = q + STAGES * G;
 
-        // stage -> FP32 tiles (masked)
-        if (MODE == MODE_FUSED) {
-            widen_box<MODE, TIn, 0, 0, 1>(stage + L::row_off(0), Af, m.n, tid);
-            widen_box<MODE, TIn, 1, 0, 2>(stage + L::row_off(1), Af, m.n, tid);
-            widen_box<MODE, TIn, 2, 0, 3>(stage + L::row_off(2), Af, m.n, tid);
-            widen_box<MODE, TIn, 3, 0, 4>(stage + L::row_off(3), Af, m.n, tid);
-        } else if (MODE == MODE_DIAG) {
-            widen_box<MODE, TIn, 0, 0, 1>(stage + L::row_off(0), Af, m.n, tid);
-            widen_box<MODE, TIn, 1, 1, 1>(stage + L::row_off(1), Af, m.n, tid);
-            widen_box<MODE, TIn, 2, 2, 1>(stage + L::row_off(2), Af, m.n, tid);
-            widen_box<MODE, TIn, 3, 3, 1>(stage + L::row_off(3), Af, m.n, tid);
-        } else {
-            widen_box<MODE, TIn, 1, 0, 1>(stage + L::row_off(1), Af, m.n, tid);
-            widen_box<MODE, TIn, 2, 0, 2>(stage + L::row_off(2), Af, m.n, tid);
-            widen_box<MODE, TIn, 3, 0, 3>(stage + L::row_off(3), Af, m.n, tid);
-            // workspace tile: 4 row-major 16x16 FP32 diagonal inverses
+        if (MODE != MODE_MERGE) store_upper_zeros(out, m, p.H, tid);
+
+        // A operands: widened copy (16-bit input) or the landing buffer itself
+        if (L::WIDEN) {
+            widen_all<MODE, TIn>(stage, Af, m.n, tid);
+        } else if (m.n < BT) {
+            zero_rows<MODE>(stage, m.n, tid);
+        }
+        if (MODE == MODE_MERGE) {
+            // workspace tile (4 row-major 16x16 FP32 inverses) -> X slots 0..3
             const float *wt = reinterpret_cast<const float *>(stage + L::WS_OFF);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const int e = tid + NTHREADS * v;          // float4 index 0..255
+                const int e = tid + NTHREADS * v;
                 const int u = e >> 6, i = (e >> 2) & 15, k4 = e & 3;
-                const float4 x = *reinterpret_cast<const float4 *>(wt + u * 256 + i * 16 + 4 * k4);
-                *reinterpret_cast<float4 *>(Xn + blk(u, u) * XBS + i * XP + 4 * k4) = x;
-                if (u < 3) {
-                    float *t = Xt + (u == 0 ? T_X00 : u == 1 ? T_X11 : T_X22) * XBS;
-                    t[(4 * k4 + 0) * XP + i] = x.x;
-                    t[(4 * k4 + 1) * XP + i] = x.y;
-                    t[(4 * k4 + 2) * XP + i] = x.z;
-                    t[(4 * k4 + 3) * XP + i] = x.w;
-                }
+                *reinterpret_cast<float4 *>(Xs + u * XBS + i * XP + 4 * k4) =
+                    *reinterpret_cast<const float4 *>(wt + u * 256 + i * 16 + 4 * k4);
             }
         }
-        __syncthreads();
-        if (tid == 0) {                      // refill the stage just drained
+        // TMA data is visible to every thread after its own mbarrier wait; a
+        // barrier is needed only when threads rewrote shared memory above.
+        if (L::WIDEN || MODE == MODE_MERGE || m.n < BT) __syncthreads();
+        if (L::WIDEN && tid == 0) {          // the landing buffer is no longer read
             fence_proxy_async();
-            issue<MODE, TIn>(p, maps.m, q + STAGES * G, walk, smem, st);
+            issue<MODE, TIn>(p, maps.m, q_next, walk, smem, st);
         }
 
         if (MODE != MODE_MERGE) {
-            const int unit = tid >> 4, j = tid & 15;
             float x[16];
-            diag_invert(Af + af_slot<MODE>(unit, unit) * ABS, j, x);
+            const int b = diag_of_unit(unit);
+            const AView a = aview<MODE, TIn>(stage, Af, b, b);
+            diag_invert(a.p, a.pitch, l, x);
+            // diagonal block of the output, one lane per column
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * b + i;
+                if (r < m.n) put1(out + (int64_t(m.row0 + r) * p.H + m.h) * BT + 16 * b + l, x[i]);
+            }
             if (MODE == MODE_DIAG) {
-                float *w = p.ws + size_t(q) * 1024 + unit * 256 + j;
+                float *w = p.ws + size_t(q) * 1024 + b * 256 + l;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) w[i * 16] = x[i];
+                if (!L::WIDEN) {
+                    __syncthreads();
+                    if (tid == 0) {
+                        fence_proxy_async();
+                        issue<MODE, TIn>(p, maps.m, q_next, walk, smem, st);
+                    }
+                }
                 continue;
             }
-            float *xn = Xn + blk(unit, unit) * XBS;
+            float *xs = Xs + b * XBS;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) xn[i * XP + j] = x[i];
-            if (unit < 3) {
-                float *t = Xt + (unit == 0 ? T_X00 : unit == 1 ? T_X11 : T_X22) * XBS + j * XP;
-#pragma unroll
-                for (int i = 0; i < 16; i += 4)
-                    *reinterpret_cast<float4 *>(t + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
-            }
-            __syncthreads();
+            for (int i = 0; i < 16; ++i) xs[i * XP + l] = x[i];
+            __syncwarp();                    // step 0 reads only this warp's inverses
         }
-        if (MODE != MODE_DIAG) {
-            merge(Af, Xn, Xt, U, tid);
-            store_tile<TOut>(reinterpret_cast<TOut *>(p.out), m, p.H, Xn, tid);
+
+        // ---- merge: four steps; U slots hold U' = -U
+        //   step 0  warp 0: U_A' = -X11 A10, U_B' = -X33 A32     warp 1: U00' = -X22 A20, U01' = -X22 A21
+        //   step 1  warp 0: X10 = U_A' X00, X32 = U_B' X22       warp 1: U10p' = -X33 A30, U11p' = -X33 A31
+        //   step 2  warp 0: X21 = U01' X11, X20p = U00' X00      warp 1: U10' = U10p' + (-X32) A20, U11' likewise
+        //   step 3  warp 0: X31 = U11' X11, X20 = X20p + U01' X10
+        //           warp 1: T = U10' X00 (unit 2), X30 = U11' X10 + T (unit 3)
+        float acc[4][4];
+        zero(acc);
+#pragma unroll 1
+        for (int step = 0; step < 4; ++step) {
+            const float *P;
+            const float *Q;
+            int qp = XP;
+            bool tri = false;
+            if (step == 0) {
+                tri = true;
+                if (warp == 0) {
+                    P = Xs + (half ? 3 : 1) * XBS;
+                    const AView a = aview<MODE, TIn>(stage, Af, half ? 3 : 1, half ? 2 : 0);
+                    Q = a.p; qp = a.pitch;
+                } else {
+                    P = Xs + 2 * XBS;
+                    const AView a = aview<MODE, TIn>(stage, Af, 2, half);
+                    Q = a.p; qp = a.pitch;
+                }
+            } else if (step == 1) {
+                if (warp == 0) {
+                    P = U + half * XBS;
+                    Q = Xs + (half ? 2 : 0) * XBS;
+                } else {
+                    tri = true;
+                    P = Xs + 3 * XBS;
+                    const AView a = aview<MODE, TIn>(stage, Af, 3, half);
+                    Q = a.p; qp = a.pitch;
+                }
+            } else if (step == 2) {
+                if (warp == 0) {
+                    P = U + (half ? 2 : 3) * XBS;                 // U00' : U01'
+                    Q = Xs + (half ? 0 : 1) * XBS;                // X00  : X11
+                } else {
+                    P = Xs + XS_32N * XBS;
+                    const AView a = aview<MODE, TIn>(stage, Af, 2, half);
+                    Q = a.p; qp = a.pitch;
+                }
+            } else {
+                if (warp == 0) {
+                    P = U + (half ? 3 : 1) * XBS;                 // U01' : U11'
+                    Q = Xs + (half ? XS_10 : 1) * XBS;            // X10  : X11
+                } else {
+                    P = U + (half ? 1 : 0) * XBS;                 // U11' : U10'
+                    Q = Xs + (half ? XS_10 : 0) * XBS;            // X10  : X00
+                }
+            }
+            if (tri) prod<true>(acc, P, Q, qp, rg, cg);
+            else prod<false>(acc, P, Q, qp, rg, cg);
+
+            if (step == 0) {
+                put_smem<false>(U + (warp == 0 ? half : 2 + half) * XBS, acc, rg, cg);
+                zero(acc);
+                __syncthreads();
+            } else if (step == 1) {
+                if (warp == 0) {             // X10 (half 0) / X32 (half 1)
+                    if (half) put_smem<true>(Xs + XS_32N * XBS, acc, rg, cg);
+                    else put_smem<false>(Xs + XS_10 * XBS, acc, rg, cg);
+                    put_out(out, m, p.H, half ? 3 : 1, half ? 2 : 0, acc, rg, cg);
+                    zero(acc);
+                }
+                __syncthreads();
+            } else if (step == 2) {
+                if (warp == 0) {
+                    if (!half) {             // X21 done; half 1 keeps X20p
+                        put_out(out, m, p.H, 2, 1, acc, rg, cg);
+                        zero(acc);
+                    }
+                } else {                     // U10' / U11'
+                    put_smem<false>(U + half * XBS, acc, rg, cg);
+                    zero(acc);
+                }
+                __syncthreads();
+                if (!L::WIDEN && tid == 0) { // A is no longer read
+                    fence_proxy_async();
+                    issue<MODE, TIn>(p, maps.m, q_next, walk, smem, st);
+                }
+            } else {
+                if (warp == 0) {             // X31 (half 0) / X20 (half 1)
+                    put_out(out, m, p.H, half ? 2 : 3, half ? 0 : 1, acc, rg, cg);
+                } else {
+                    if (!half) put_smem<false>(U + 2 * XBS, acc, rg, cg);   // T
+                    __syncwarp();
+                    if (half) {              // X30 = U11' X10 + T
+                        const float *t = U + 2 * XBS;
+#pragma unroll
+                        for (int mm = 0; mm < 4; ++mm) {
+                            const float4 v = *reinterpret_cast<const float4 *>(t + (rg + 4 * mm) * XP + 4 * cg);
+                            acc[mm][0] += v.x; acc[mm][1] += v.y; acc[mm][2] += v.z; acc[mm][3] += v.w;
+                        }
+                        put_out(out, m, p.H, 3, 0, acc, rg, cg);
+                    }
+                }
+            }
         }
     }
 }

@@ -51,7 +51,13 @@ cudaError_t launch_one(const Maps &maps, const Params &p, int device, int num_sm
 template <typename TIn>
 cudaError_t launch_in(int mode, int out_dtype, const Maps &maps, const Params &p, int device, int num_sms,
                       cudaStream_t stream) {
-    if (mode == MODE_DIAG) return launch_one<MODE_DIAG, TIn, float>(maps, p, device, num_sms, stream);
+    if (mode == MODE_DIAG) {        // writes the diagonal and zero blocks of the output too
+        switch (out_dtype) {
+            case 0: return launch_one<MODE_DIAG, TIn, float>(maps, p, device, num_sms, stream);
+            case 1: return launch_one<MODE_DIAG, TIn, __nv_bfloat16>(maps, p, device, num_sms, stream);
+            default: return launch_one<MODE_DIAG, TIn, __half>(maps, p, device, num_sms, stream);
+        }
+    }
     if (mode == MODE_FUSED) {
         switch (out_dtype) {
             case 0: return launch_one<MODE_FUSED, TIn, float>(maps, p, device, num_sms, stream);
