@@ -86,9 +86,13 @@ typedef enum {
     KDA_PATH_SINGLE = 2           /* one kernel, no workspace */
 } kda_path_t;
 
-/* Smallest T (total rows) for which the selector takes the split path
- * ("minimum input length", same PR description). */
-#define KDA_SPLIT_MIN_TOKENS 4096
+/* Smallest B*T (total rows) for which the selector takes the split path
+ * ("minimum input length", same PR description).  Set from GB300
+ * measurements: the single-pass kernel already inverts the four diagonal
+ * blocks in parallel inside one CTA, so splitting only adds the workspace round
+ * trip and a launch, and it was slower at every size measured (64 to 131072
+ * rows); the threshold therefore lies above any size this build supports. */
+#define KDA_SPLIT_MIN_TOKENS (INT64_C(1) << 32)
 
 /*
  * Workspace bytes the split path needs for this shape: KDA_WS_TILE_BYTES per

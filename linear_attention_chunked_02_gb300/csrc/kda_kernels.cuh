@@ -459,14 +459,17 @@ __device__ __forceinline__ void prod(float (&acc)[4][4], const float *__restrict
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const float4 qv = *reinterpret_cast<const float4 *>(Q + (4 * q + kk) * qp + 4 * cg);
+            const float2 q01 = make_float2(qv.x, qv.y), q23 = make_float2(qv.z, qv.w);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 if (TRI_NEG && m < q) continue;
                 const float a = TRI_NEG ? -comp(pr[m], kk) : comp(pr[m], kk);
-                acc[m][0] = fmaf(a, qv.x, acc[m][0]);
-                acc[m][1] = fmaf(a, qv.y, acc[m][1]);
-                acc[m][2] = fmaf(a, qv.z, acc[m][2]);
-                acc[m][3] = fmaf(a, qv.w, acc[m][3]);
+                const float2 aa = make_float2(a, a);
+                // two FMAs per instruction; each component rounds exactly like fmaf
+                float2 c01 = __ffma2_rn(aa, q01, make_float2(acc[m][0], acc[m][1]));
+                float2 c23 = __ffma2_rn(aa, q23, make_float2(acc[m][2], acc[m][3]));
+                acc[m][0] = c01.x; acc[m][1] = c01.y;
+                acc[m][2] = c23.x; acc[m][3] = c23.y;
             }
         }
     }
@@ -489,23 +492,21 @@ __device__ __forceinline__ void put_smem(float *dst, const float (&acc)[4][4], i
             make_float4(s * acc[m][0], s * acc[m][1], s * acc[m][2], s * acc[m][3]);
 }
 
-// tile -> output block (bi, bj) of the chunk, rows below n only
+// tile -> output block (bi, bj) of the chunk, rows below n only.  `ob` points
+// at the chunk-head's first output row, `os` is the row stride (H * 64).
 template <typename TOut>
-__device__ __forceinline__ void put_out(TOut *out, const Meta &m, int H, int bi, int bj,
-                                        const float (&acc)[4][4], int rg, int cg) {
+__device__ __forceinline__ void put_out(TOut *ob, int os, int n, int bi, int bj, const float (&acc)[4][4],
+                                        int rg, int cg) {
 #pragma unroll
     for (int mm = 0; mm < 4; ++mm) {
         const int r = 16 * bi + rg + 4 * mm;
-        if (r < m.n) {
-            TOut *dst = out + (int64_t(m.row0 + r) * H + m.h) * BT + 16 * bj + 4 * cg;
-            put4(dst, acc[mm][0], acc[mm][1], acc[mm][2], acc[mm][3]);
-        }
+        if (r < n) put4(ob + (r * os + 16 * bj + 4 * cg), acc[mm][0], acc[mm][1], acc[mm][2], acc[mm][3]);
     }
 }
 
 // The zero blocks above the diagonal (columns 16(br+1) .. 63 of rows in block-row br).
 template <typename TOut>
-__device__ __forceinline__ void store_upper_zeros(TOut *out, const Meta &m, int H, int tid) {
+__device__ __forceinline__ void store_upper_zeros(TOut *ob, int os, int n, int tid) {
     constexpr int VEC = 16 / int(sizeof(TOut));     // elements per 16-byte store
     constexpr int PB = 16 / VEC;                    // 16-byte stores per 16-column block
 #pragma unroll
@@ -518,10 +519,7 @@ __device__ __forceinline__ void store_upper_zeros(TOut *out, const Meta &m, int 
             if (e < cnt) {
                 const int r = 16 * br + e / per_row;
                 const int c = 16 * (br + 1) + VEC * (e % per_row);
-                if (r < m.n) {
-                    TOut *dst = out + (int64_t(m.row0 + r) * H + m.h) * BT + c;
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-                }
+                if (r < n) *reinterpret_cast<uint4 *>(ob + (r * os + c)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
     }
@@ -578,8 +576,10 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         unsigned char *stage = smem + L::OFF_STAGE + st * L::STAGE_BYTES;
         const int32_t q = int32_t(blockIdx.x) + it * G;
         const int32_t q_next = q + STAGES * G;
+        const int os = p.H * BT;                                  // output row stride
+        TOut *ob = out + (int64_t(m.row0) * p.H + m.h) * BT;      // chunk-head's first row
 
-        if (MODE != MODE_MERGE) store_upper_zeros(out, m, p.H, tid);
+        if (MODE != MODE_MERGE) store_upper_zeros(ob, os, m.n, tid);
 
         // A operands: widened copy (16-bit input) or the landing buffer itself
         if (L::WIDEN) {
@@ -615,7 +615,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = 16 * b + i;
-                if (r < m.n) put1(out + (int64_t(m.row0 + r) * p.H + m.h) * BT + 16 * b + l, x[i]);
+                if (r < m.n) put1(ob + (r * os + 16 * b + l), x[i]);
             }
             if (MODE == MODE_DIAG) {
                 float *w = p.ws + size_t(q) * 1024 + b * 256 + l;
@@ -700,14 +700,14 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
                 if (warp == 0) {             // X10 (half 0) / X32 (half 1)
                     if (half) put_smem<true>(Xs + XS_32N * XBS, acc, rg, cg);
                     else put_smem<false>(Xs + XS_10 * XBS, acc, rg, cg);
-                    put_out(out, m, p.H, half ? 3 : 1, half ? 2 : 0, acc, rg, cg);
+                    put_out(ob, os, m.n, half ? 3 : 1, half ? 2 : 0, acc, rg, cg);
                     zero(acc);
                 }
                 __syncthreads();
             } else if (step == 2) {
                 if (warp == 0) {
                     if (!half) {             // X21 done; half 1 keeps X20p
-                        put_out(out, m, p.H, 2, 1, acc, rg, cg);
+                        put_out(ob, os, m.n, 2, 1, acc, rg, cg);
                         zero(acc);
                     }
                 } else {                     // U10' / U11'
@@ -721,7 +721,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
             } else {
                 if (warp == 0) {             // X31 (half 0) / X20 (half 1)
-                    put_out(out, m, p.H, half ? 2 : 3, half ? 0 : 1, acc, rg, cg);
+                    put_out(ob, os, m.n, half ? 2 : 3, half ? 0 : 1, acc, rg, cg);
                 } else {
                     if (!half) put_smem<false>(U + 2 * XBS, acc, rg, cg);   // T
                     __syncwarp();
@@ -732,7 +732,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
                             const float4 v = *reinterpret_cast<const float4 *>(t + (rg + 4 * mm) * XP + 4 * cg);
                             acc[mm][0] += v.x; acc[mm][1] += v.y; acc[mm][2] += v.z; acc[mm][3] += v.w;
                         }
-                        put_out(out, m, p.H, 3, 0, acc, rg, cg);
+                        put_out(ob, os, m.n, 3, 0, acc, rg, cg);
                     }
                 }
             }

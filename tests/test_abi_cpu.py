@@ -47,20 +47,25 @@ def test_workspace_size_and_selector(L):
     assert kda.workspace_size(1, 5, 1, 5) == 5 * 4096          # capped by T
     assert kda.workspace_size(0, 0, 1, 0) == 0
     assert kda.workspace_size(2, 64, 1, 3) == 0                # packed needs B == 1
+    # GB300 selector: the split path never paid at measured sizes, so AUTO is
+    # single pass below the minimum length whatever the workspace
     need = kda.workspace_size(1, 8192, 64, 16)
-    assert kda.select_path(1, 8192, 64, 16, need) == "split"
-    assert kda.select_path(1, 8192, 64, 16, need - 1) == "single"
-    assert kda.select_path(1, 8192, 64, 16, 0) == "single"
-    assert kda.select_path(1, 64, 64, 0, 1 << 30) == "single"  # below the minimum length
+    assert kda.select_path(1, 8192, 64, 16, need) == "single"
+    assert kda.select_path(1, 64, 64, 0, 1 << 30) == "single"
+    # the budget rule itself, above the minimum length (pure host arithmetic)
+    T = 1 << 32
+    need = kda.workspace_size(1, T, 8, 4096)
+    assert kda.select_path(1, T, 8, 4096, need) == "split"
+    assert kda.select_path(1, T, 8, 4096, need - 1) == "single"
+    assert kda.select_path(1, T, 8, 4096, 0) == "single"
     # occupancy < 16 rows per chunk: the workspace would exceed the FP32 input
-    T, N = 8192, 4096                                          # requests of 2 rows
-    assert kda.select_path(1, T, 8, N, 1 << 40) == "single"
-    # the bound counts a possibly partial chunk per request, so 16-row requests
-    # (632 chunks bounded vs 512 real) already exceed it; 32-row requests do not
-    T, N = 8192, 512
-    assert kda.select_path(1, T, 8, N, 1 << 40) == "single"
-    T, N = 8192, 256
-    assert kda.select_path(1, T, 8, N, 1 << 40) == "split"
+    N = (1 << 30) - 1                                          # requests of ~4 rows
+    assert kda.workspace_size(1, T, 8, N) > T * 8 * 256
+    assert kda.select_path(1, T, 8, N, 1 << 62) == "single"
+    # the bound counts a possibly partial chunk per request, so 16-row
+    # requests already exceed it while 32-row requests do not
+    assert kda.select_path(1, T, 8, T // 16, 1 << 62) == "single"
+    assert kda.select_path(1, T, 8, T // 32, 1 << 62) == "split"
 
 
 def call(L, A=16, Ai=1 << 20, cu=None, nseq=0, B=1, T=64, H=1, ind=0, outd=0, ws=None, wsb=0, path=0):
