@@ -73,8 +73,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// A viewed as a 3-D tensor {64 columns, H heads, rows}; box {16w, 1, 16}.
-bool make_maps(const void *A, int32_t dt, int32_t H, int64_t rows, kda::Maps &maps) {
+// A tensor [rows, H, 64] viewed as 3-D {64 columns, H heads, rows}, with boxes of
+// {16 (w+1) columns, 1 head, 16 rows} for w = 0 .. n-1.
+bool encode_maps(const void *base, int32_t dt, int32_t H, int64_t rows, CUtensorMap *maps, int n) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const CUtensorMapDataType ty = dt == KDA_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -84,14 +85,20 @@ bool make_maps(const void *A, int32_t dt, int32_t H, int64_t rows, kda::Maps &ma
     const cuuint64_t dims[3] = {cuuint64_t(kda::BT), cuuint64_t(H), cuuint64_t(rows)};
     const cuuint64_t strides[2] = {kda::BT * es, cuuint64_t(H) * kda::BT * es};
     const cuuint32_t estr[3] = {1, 1, 1};
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < n; ++w) {
         const cuuint32_t box[3] = {cuuint32_t(16 * (w + 1)), 1, 16};
-        CUresult r = fn(&maps.m[w], ty, 3, const_cast<void *>(A), dims, strides, box, estr,
+        CUresult r = fn(&maps[w], ty, 3, const_cast<void *>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return false;
     }
     return true;
+}
+
+// Input boxes (A, widths 16..64) and output boxes (Ai, widths 16..48, used to
+// store the zero blocks above the diagonal of full chunks).
+bool make_maps(const void *A, int32_t in_dt, void *Ai, int32_t out_dt, int32_t H, int64_t rows, kda::Maps &maps) {
+    return encode_maps(A, in_dt, H, rows, maps.m, 4) && encode_maps(Ai, out_dt, H, rows, maps.o, 3);
 }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
@@ -180,7 +187,7 @@ kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *cu_seqlen
     kda::Maps maps;
     std::memset(&maps, 0, sizeof(maps));
     const int64_t rows = B * T;
-    if (!make_maps(A, in_dtype, H, rows, maps)) return KDA_ERR_CUDA;
+    if (!make_maps(A, in_dtype, Ai, out_dtype, H, rows, maps)) return KDA_ERR_CUDA;
 
     kda::Params p;
     p.out = Ai;

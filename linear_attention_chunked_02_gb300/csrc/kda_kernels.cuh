@@ -19,21 +19,21 @@
 //     substitution in registers (FP32 FMA).
 //   * Merge, as two 32x32 levels (the 64x64 matrix is lower block-triangular
 //     with 32x32 blocks TL, BR and off-diagonal BL):
-//        level A: X10 = -(X11 A10) X00,  X32 = -(X33 A32) X22
-//        level B: U = X_BR A_BL,  X_BL = -U X_TL
-//     which is Linv_ij = -Linv_ii sum_k A_ik Linv_kj regrouped.  Each 16x16x16
-//     FP32 product is computed by one unit with a 4x4 register tile per lane.
-//     The U blocks are kept negated (U' = -U), so only two product kinds
-//     exist: "lower-triangular left factor, negated" (which skips the k-quads
-//     where the diagonal inverse is structurally zero) and "dense".  The
-//     products run as a 4-step loop over a fixed schedule in which all four
-//     units are busy in every step; one call site per product kind keeps the
-//     code small enough for the instruction cache.
-//   * Every output block is stored straight from the registers that computed
-//     it (16-byte row segments), the zero blocks above the diagonal directly.
+//        level A: X10 = -X11 A10 X00,  X32 = -X33 A32 X22
+//        level B: T = A_BL X_TL,  X_BL = -X_BR T
+//     which is Linv_ij = -Linv_ii sum_k A_ik Linv_kj regrouped.  The 16x16x16
+//     products run on the tensor cores (mma.sync TF32, split into hi + lo
+//     parts so the result keeps FP32 accuracy) and are computed transposed
+//     (T^T = X_TL^T A_BL^T, X_BL^T = T^T (-X_BR)^T): A is then read row-major
+//     straight from the landing buffer, and each intermediate T stays in
+//     registers as the next product's left operand.  One barrier per chunk-head.
+//   * Every output block is stored from the registers that computed it; the
+//     zero blocks above the diagonal of full chunks are TMA tensor stores from
+//     a zeroed shared-memory buffer.
 //   * Split path: MODE_DIAG inverts the diagonal blocks, writes them (and the
-//     zero blocks) to the output and their FP32 tiles to the workspace;
-//     MODE_MERGE loads the tiles back and produces the off-diagonal blocks.
+//     zero blocks) to the output and their transposed FP32 tiles to the
+//     workspace; MODE_MERGE loads the tiles back and produces the
+//     off-diagonal blocks.
 //     Both call the same device functions as MODE_FUSED, so every element is
 //     computed with the same operations in the same order.
 #pragma once
@@ -54,21 +54,21 @@ constexpr int MODE_FUSED = 0;
 constexpr int MODE_DIAG = 1;
 constexpr int MODE_MERGE = 2;
 
-// On-chip FP32 tiles.  X / U blocks: pitch 20 floats (rows 4 apart land in
-// distinct bank quads), block stride 336 floats.  Widened 16-bit A blocks:
-// pitch 16, block stride 272 floats.
-constexpr int XP = 20;
-constexpr int XBS = 336;
+// On-chip FP32 tiles.  Widened 16-bit A blocks: pitch 16, block stride 272
+// floats.  X tiles: "Xt" slots hold transposed inverse blocks row-major with
+// pitch 16 (left operands, one 16-byte load per fragment row), "Xr" slots hold
+// negated inverse blocks row-major with pitch 24 (right operands, 8-byte loads
+// that fall in distinct banks).
 constexpr int AP16 = 16;
 constexpr int ABS = 272;
+constexpr int XTP = 16, XTS = 256;     // Xt pitch / slot stride (floats)
+constexpr int XRP = 24, XRS = 384;     // Xr pitch / slot stride (floats)
 
 __host__ __device__ constexpr int blk(int i, int j) { return i * (i + 1) / 2 + j; }
 
-// X slots 0..3 hold the diagonal inverses X00..X33; slot 4 X10, slot 5 -X32.
-constexpr int XS_10 = 4, XS_32N = 5;
-// Diagonal block inverted by each unit: warp 0 takes X11 and X33, warp 1 X00
-// and X22, so that the first merge step only needs the unit's own warp.
-__host__ __device__ constexpr int diag_of_unit(int u) { return u == 0 ? 1 : u == 1 ? 3 : u == 2 ? 0 : 2; }
+// Xt slots: X00^T, X22^T, X11^T, X10^T.  Xr slots: -X11, -X33, -X22, -X32.
+constexpr int XT_00 = 0, XT_22 = 1, XT_11 = 2, XT_10 = 3;
+constexpr int XR_11 = 0, XR_33 = 1, XR_22 = 2, XR_32 = 3;
 
 // device-side error word (bit 0: a bounded TMA wait ran out)
 constexpr unsigned ERR_WAIT_TIMEOUT = 1u;
@@ -155,6 +155,22 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// TMA tile store from shared memory (bulk async-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until every committed bulk group has completed (writes included).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // --------------------------------------------------------- dtype helpers
 template <typename T> struct Elt;
 template <> struct Elt<float> {
@@ -225,15 +241,20 @@ struct Layout {
     static constexpr int STAGE_BYTES = MODE == MODE_MERGE ? WS_OFF + 4096 : WS_OFF;
     static constexpr uint32_t TX_BYTES = MODE == MODE_MERGE ? A_BYTES + 4096 : A_BYTES;
     static constexpr int NAF = WIDEN ? (MODE == MODE_DIAG ? 4 : 10) : 0;   // widened A-block slots
-    static constexpr int NX = MODE == MODE_DIAG ? 0 : 6;
-    static constexpr int NU = MODE == MODE_DIAG ? 0 : 4;
+    static constexpr int X_BYTES = MODE == MODE_DIAG ? 0 : 4 * (4 * XTS + 4 * XRS);
     static constexpr int OFF_BAR = 0;
     static constexpr int OFF_META = 64;
     static constexpr int OFF_STAGE = 128;
     static constexpr int OFF_AF = OFF_STAGE + STAGES * STAGE_BYTES;
-    static constexpr int OFF_X = OFF_AF + NAF * ABS * 4;
-    static constexpr int OFF_U = OFF_X + NX * XBS * 4;
-    static constexpr int BYTES = OFF_U + NU * XBS * 4;
+    static constexpr int OFF_XT = OFF_AF + NAF * ABS * 4;
+    static constexpr int OFF_XR = OFF_XT + (MODE == MODE_DIAG ? 0 : 4 * XTS * 4);
+    // 16 x 48 zero elements (FP32-sized) that TMA stores copy into the blocks
+    // above the diagonal of full chunks
+    static constexpr int Z_BYTES = MODE == MODE_MERGE ? 0 : 16 * 48 * 4;
+    static constexpr int OFF_Z = OFF_XT + X_BYTES;
+    static constexpr int BYTES = OFF_Z + Z_BYTES;
+    static_assert(OFF_Z % 128 == 0 && OFF_STAGE % 128 == 0 && STAGE_BYTES % 128 == 0,
+                  "TMA source/destination buffers must be 128-byte aligned");
     // stage offset (bytes) of block-row r's box, and the box width in elements
     __host__ __device__ static constexpr int row_off(int r) {
         return MODE == MODE_FUSED ? 256 * ELT * (r * (r + 1) / 2)
@@ -436,72 +457,145 @@ __device__ __forceinline__ void diag_invert(const float *a, int ap, int j, float
     }
 }
 
-// ----------------------------------------------------------- 16x16 products
-// A unit computes a 16x16 tile; lane l (0..15): rg = l >> 2, cg = l & 3.
-// acc[m][n] is row rg + 4m, column 4cg + n.
+// ------------------------------------------------------ tensor-core products
+// 16x16x16 products on mma.sync m16n8k8 (TF32 in, FP32 accumulate) in split
+// precision: an FP32 operand x = hi + lo with hi = x truncated to TF32 and lo =
+// (x - hi) truncated to TF32, and P Q ~ Pl Qh + Ph Ql + Ph Qh (the dropped Pl Ql
+// is ~2^-22 relative).  Operands exact in TF32 (widened bf16 / fp16 input) skip
+// their lo term.
+//
+// m16n8k8 fragments (lane = 4 g + t): A a0 = A[g][s], a1 = A[g+8][s], a2 =
+// A[g][s'], a3 = A[g+8][s']; B b0 = B[s][n], b1 = B[s'][n] with n = g; C c0 =
+// C[g][2t], c1 = C[g][2t+1], c2 = C[g+8][2t], c3 = C[g+8][2t+1]; s, s' are the
+// k-slots t, t+4.  The contraction index a k-slot stands for is free as long as
+// A and B agree; two assignments are used:
+//   kperm4: k-step 0 slots -> k = 4t, 4t+1; k-step 1 -> 4t+2, 4t+3
+//           (left operand read with one 16-byte load per fragment row)
+//   kperm2: k-step 0 slots -> k = 2t, 2t+1; k-step 1 -> 8+2t, 9+2t
+//           (left operand taken from a previous product's C fragments)
+struct TileA { uint32_t h[2][4], l[2][4]; };      // [k-step][a0..a3]
+struct TileB { uint32_t h[2][2][2], l[2][2][2]; };  // [k-step][n-tile][b0, b1]
+struct TileC { float c[2][4]; };                   // [n-tile][c0..c3]
 
-__device__ __forceinline__ float comp(const float4 &v, int kk) {
-    return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
+__device__ __forceinline__ void split_tf32(float v, uint32_t &h, uint32_t &l) {
+    const uint32_t b = __float_as_uint(v) & 0xffffe000u;
+    h = b;
+    l = __float_as_uint(v - __uint_as_float(b)) & 0xffffe000u;
 }
 
-// TRI_NEG = false: acc += P Q.  TRI_NEG = true: acc -= P Q with P lower
-// triangular, so k-quad q only meets rows m >= q (the negation is folded into
-// the FMA operand).  P row-major with pitch XP, Q row-major with pitch qp.
-template <bool TRI_NEG>
-__device__ __forceinline__ void prod(float (&acc)[4][4], const float *__restrict__ P,
-                                     const float *__restrict__ Q, int qp, int rg, int cg) {
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void zero(TileC &c) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        float4 pr[4];
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-            if (!TRI_NEG || m >= q) pr[m] = *reinterpret_cast<const float4 *>(P + (rg + 4 * m) * XP + 4 * q);
+        for (int i = 0; i < 4; ++i) c.c[nt][i] = 0.f;
+}
+
+// Left operand (kperm4): row-major 16x16 tile at p with pitch lp.
+__device__ __forceinline__ void left_smem(TileA &a, const float *p, int lp, int g, int t) {
+    const float4 r0 = *reinterpret_cast<const float4 *>(p + g * lp + 4 * t);
+    const float4 r1 = *reinterpret_cast<const float4 *>(p + (g + 8) * lp + 4 * t);
+    split_tf32(r0.x, a.h[0][0], a.l[0][0]); split_tf32(r1.x, a.h[0][1], a.l[0][1]);
+    split_tf32(r0.y, a.h[0][2], a.l[0][2]); split_tf32(r1.y, a.h[0][3], a.l[0][3]);
+    split_tf32(r0.z, a.h[1][0], a.l[1][0]); split_tf32(r1.z, a.h[1][1], a.l[1][1]);
+    split_tf32(r0.w, a.h[1][2], a.l[1][2]); split_tf32(r1.w, a.h[1][3], a.l[1][3]);
+}
+
+// Left operand (kperm2): the C fragments of a previous 16x16 product.
+__device__ __forceinline__ void left_regs(TileA &a, const TileC &c) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const float4 qv = *reinterpret_cast<const float4 *>(Q + (4 * q + kk) * qp + 4 * cg);
-            const float2 q01 = make_float2(qv.x, qv.y), q23 = make_float2(qv.z, qv.w);
+    for (int ks = 0; ks < 2; ++ks) {
+        split_tf32(c.c[ks][0], a.h[ks][0], a.l[ks][0]);
+        split_tf32(c.c[ks][2], a.h[ks][1], a.l[ks][1]);
+        split_tf32(c.c[ks][1], a.h[ks][2], a.l[ks][2]);
+        split_tf32(c.c[ks][3], a.h[ks][3], a.l[ks][3]);
+    }
+}
+
+// Right operand Q = R^T (kperm4) for row-major R at r with pitch rp; EXACT: R
+// holds TF32-exact values (no lo part).
+template <bool EXACT>
+__device__ __forceinline__ void right4(TileB &b, const float *r, int rp, int g, int t) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (TRI_NEG && m < q) continue;
-                const float a = TRI_NEG ? -comp(pr[m], kk) : comp(pr[m], kk);
-                const float2 aa = make_float2(a, a);
-                // two FMAs per instruction; each component rounds exactly like fmaf
-                float2 c01 = __ffma2_rn(aa, q01, make_float2(acc[m][0], acc[m][1]));
-                float2 c23 = __ffma2_rn(aa, q23, make_float2(acc[m][2], acc[m][3]));
-                acc[m][0] = c01.x; acc[m][1] = c01.y;
-                acc[m][2] = c23.x; acc[m][3] = c23.y;
-            }
+    for (int nt = 0; nt < 2; ++nt) {
+        const float4 v = *reinterpret_cast<const float4 *>(r + (8 * nt + g) * rp + 4 * t);
+        if (EXACT) {
+            b.h[0][nt][0] = __float_as_uint(v.x); b.h[0][nt][1] = __float_as_uint(v.y);
+            b.h[1][nt][0] = __float_as_uint(v.z); b.h[1][nt][1] = __float_as_uint(v.w);
+        } else {
+            split_tf32(v.x, b.h[0][nt][0], b.l[0][nt][0]); split_tf32(v.y, b.h[0][nt][1], b.l[0][nt][1]);
+            split_tf32(v.z, b.h[1][nt][0], b.l[1][nt][0]); split_tf32(v.w, b.h[1][nt][1], b.l[1][nt][1]);
         }
     }
 }
 
-__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+// Right operand Q = R^T (kperm2) for row-major R at r with pitch rp.
+__device__ __forceinline__ void right2(TileB &b, const float *r, int rp, int g, int t) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
+        for (int ks = 0; ks < 2; ++ks) {
+            const float2 v = *reinterpret_cast<const float2 *>(r + (8 * nt + g) * rp + 8 * ks + 2 * t);
+            split_tf32(v.x, b.h[ks][nt][0], b.l[ks][nt][0]);
+            split_tf32(v.y, b.h[ks][nt][1], b.l[ks][nt][1]);
+        }
 }
 
-// (+/-) tile -> row-major X/U block
-template <bool NEG>
-__device__ __forceinline__ void put_smem(float *dst, const float (&acc)[4][4], int rg, int cg) {
-    const float s = NEG ? -1.f : 1.f;
+// c += P Q in split TF32 (B_EXACT: Q has no lo part).
+template <bool B_EXACT>
+__device__ __forceinline__ void mma_tile(TileC &c, const TileA &a, const TileB &b) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-        *reinterpret_cast<float4 *>(dst + (rg + 4 * m) * XP + 4 * cg) =
-            make_float4(s * acc[m][0], s * acc[m][1], s * acc[m][2], s * acc[m][3]);
+    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            mma8(c.c[nt], a.l[ks], b.h[ks][nt][0], b.h[ks][nt][1]);
+            if (!B_EXACT) mma8(c.c[nt], a.h[ks], b.l[ks][nt][0], b.l[ks][nt][1]);
+            mma8(c.c[nt], a.h[ks], b.h[ks][nt][0], b.h[ks][nt][1]);
+        }
 }
 
-// tile -> output block (bi, bj) of the chunk, rows below n only.  `ob` points
-// at the chunk-head's first output row, `os` is the row stride (H * 64).
+// C tile holding Y^T -> output block (bi, bj) of the chunk (rows below n only).
 template <typename TOut>
-__device__ __forceinline__ void put_out(TOut *ob, int os, int n, int bi, int bj, const float (&acc)[4][4],
-                                        int rg, int cg) {
+__device__ __forceinline__ void out_tile_t(TOut *ob, int os, int n, int bi, int bj, const TileC &c, int g, int t) {
+    const bool full = n == BT;
 #pragma unroll
-    for (int mm = 0; mm < 4; ++mm) {
-        const int r = 16 * bi + rg + 4 * mm;
-        if (r < n) put4(ob + (r * os + 16 * bj + 4 * cg), acc[mm][0], acc[mm][1], acc[mm][2], acc[mm][3]);
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 16 * bi + 8 * nt + 2 * t + e;
+            if (full || r < n) {
+                TOut *row = ob + (r * os + 16 * bj + g);
+                put1(row, c.c[nt][e]);
+                put1(row + 8, c.c[nt][2 + e]);
+            }
+        }
+}
+
+// C tile holding Y^T -> Y^T row-major (pitch XTP) in shared memory.
+__device__ __forceinline__ void smem_tile_t(float *dst, const TileC &c, int g, int t) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        *reinterpret_cast<float2 *>(dst + g * XTP + 8 * nt + 2 * t) = make_float2(c.c[nt][0], c.c[nt][1]);
+        *reinterpret_cast<float2 *>(dst + (g + 8) * XTP + 8 * nt + 2 * t) = make_float2(c.c[nt][2], c.c[nt][3]);
     }
+}
+
+// C tile holding Y^T -> -Y row-major (pitch XRP) in shared memory.
+__device__ __forceinline__ void smem_tile_neg(float *dst, const TileC &c, int g, int t) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 8 * nt + 2 * t + e;
+            dst[r * XRP + g] = -c.c[nt][e];
+            dst[r * XRP + g + 8] = -c.c[nt][2 + e];
+        }
 }
 
 // The zero blocks above the diagonal (columns 16(br+1) .. 63 of rows in block-row br).
@@ -527,33 +621,41 @@ __device__ __forceinline__ void store_upper_zeros(TOut *ob, int os, int n, int t
 
 // ----------------------------------------------------------------- kernel
 struct Maps {
-    CUtensorMap m[4];          // box widths 16, 32, 48, 64 columns; 16 rows; 1 head
+    CUtensorMap m[4];          // A: box widths 16, 32, 48, 64 columns; 16 rows; 1 head
+    CUtensorMap o[3];          // Ai: box widths 16, 32, 48 columns; 16 rows; 1 head
 };
 
 template <int MODE, typename TIn, typename TOut>
-__global__ void __launch_bounds__(NTHREADS)
+__global__ void __launch_bounds__(NTHREADS, MODE == MODE_DIAG ? 1 : 6)
 kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     using L = Layout<MODE, TIn>;
+    constexpr bool AX = L::WIDEN;            // A values exact in TF32
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     const Meta *metas = reinterpret_cast<const Meta *>(smem + L::OFF_META);
     float *Af = reinterpret_cast<float *>(smem + L::OFF_AF);
-    float *Xs = reinterpret_cast<float *>(smem + L::OFF_X);
-    float *U = reinterpret_cast<float *>(smem + L::OFF_U);
+    float *Xt = reinterpret_cast<float *>(smem + L::OFF_XT);
+    float *Xr = reinterpret_cast<float *>(smem + L::OFF_XR);
     TOut *out = reinterpret_cast<TOut *>(p.out);
     const int tid = threadIdx.x;
-    const int unit = tid >> 4, warp = tid >> 5, half = unit & 1;
-    const int l = tid & 15, rg = l >> 2, cg = l & 3;
+    const int unit = tid >> 4, warp = tid >> 5;
+    const int l = tid & 15;                  // lane in the 16-lane unit (diagonal inverse)
+    const int lane = tid & 31, g = lane >> 2, t = lane & 3;   // mma fragment coordinates
     const int32_t G = gridDim.x;
+    const int os = p.H * BT;                 // output row stride (elements)
     Walk walk{0, 0};
 
+    if (MODE != MODE_MERGE) {                // zero source of the TMA stores
+        float4 *z = reinterpret_cast<float4 *>(smem + L::OFF_Z);
+        for (int i = tid; i < L::Z_BYTES / 16; i += NTHREADS) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
-        fence_proxy_async();
         for (int s = 0; s < STAGES; ++s)
             issue<MODE, TIn>(p, maps.m, int32_t(blockIdx.x) + s * G, walk, smem, s);
     }
+    fence_proxy_async();                     // zero buffer visible to the TMA engine
     __syncthreads();
 
     for (int it = 0;; ++it) {
@@ -568,6 +670,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
                 mbar_wait_bounded(&bars[st], parity);
                 for (int s = 1; s < STAGES; ++s)
                     mbar_wait_bounded(&bars[(st + s) % STAGES], ((it + s) / STAGES) & 1);
+                bulk_wait_all();
             }
             return;
         }
@@ -575,11 +678,27 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         if (!m.valid) break;
         unsigned char *stage = smem + L::OFF_STAGE + st * L::STAGE_BYTES;
         const int32_t q = int32_t(blockIdx.x) + it * G;
-        const int32_t q_next = q + STAGES * G;
-        const int os = p.H * BT;                                  // output row stride
+        // Every thread is past the previous chunk-head, so the stage it used is
+        // free: prefetch the next chunk-head into it (one iteration ahead).
+        if (it >= 1 && tid == 0) {
+            fence_proxy_async();
+            issue<MODE, TIn>(p, maps.m, q + G, walk, smem, (it + 1) % STAGES);
+        }
         TOut *ob = out + (int64_t(m.row0) * p.H + m.h) * BT;      // chunk-head's first row
 
-        if (MODE != MODE_MERGE) store_upper_zeros(ob, os, m.n, tid);
+        if (MODE != MODE_MERGE) {            // zero blocks above the diagonal
+            if (m.n == BT) {
+                if (tid == 0) {
+#pragma unroll
+                    for (int br = 0; br < 3; ++br)
+                        tma_store_3d(&maps.o[2 - br], smem + L::OFF_Z, 16 * (br + 1), m.h, m.row0 + 16 * br);
+                    bulk_commit();
+                    bulk_wait_read<2>();
+                }
+            } else {
+                store_upper_zeros(ob, os, m.n, tid);
+            }
+        }
 
         // A operands: widened copy (16-bit input) or the landing buffer itself
         if (L::WIDEN) {
@@ -587,157 +706,125 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         } else if (m.n < BT) {
             zero_rows<MODE>(stage, m.n, tid);
         }
+        // X00^T, X11^T, X22^T: the workspace tile (MODE_MERGE) or the Xt slots
+        const float *xt00, *xt11, *xt22;
         if (MODE == MODE_MERGE) {
-            // workspace tile (4 row-major 16x16 FP32 inverses) -> X slots 0..3
+            // the workspace tile holds X00^T .. X33^T row-major; the negated
+            // inverses -X11, -X33, -X22 are transposed out of it
             const float *wt = reinterpret_cast<const float *>(stage + L::WS_OFF);
+            xt00 = wt; xt11 = wt + 256; xt22 = wt + 512;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int e = tid + NTHREADS * v;
-                const int u = e >> 6, i = (e >> 2) & 15, k4 = e & 3;
-                *reinterpret_cast<float4 *>(Xs + u * XBS + i * XP + 4 * k4) =
-                    *reinterpret_cast<const float4 *>(wt + u * 256 + i * 16 + 4 * k4);
+            for (int v = 0; v < 3; ++v) {
+                const int e = tid + NTHREADS * v;       // float4 index in blocks 1..3
+                const int b = 1 + (e >> 6), j = (e >> 2) & 15, i4 = 4 * (e & 3);
+                const float4 x = *reinterpret_cast<const float4 *>(wt + b * 256 + j * 16 + i4);
+                float *d = Xr + (b == 1 ? XR_11 : b == 3 ? XR_33 : XR_22) * XRS + j;
+                d[(i4 + 0) * XRP] = -x.x; d[(i4 + 1) * XRP] = -x.y;
+                d[(i4 + 2) * XRP] = -x.z; d[(i4 + 3) * XRP] = -x.w;
             }
+        } else {
+            xt00 = Xt + XT_00 * XTS; xt11 = Xt + XT_11 * XTS; xt22 = Xt + XT_22 * XTS;
         }
         // TMA data is visible to every thread after its own mbarrier wait; a
         // barrier is needed only when threads rewrote shared memory above.
         if (L::WIDEN || MODE == MODE_MERGE || m.n < BT) __syncthreads();
-        if (L::WIDEN && tid == 0) {          // the landing buffer is no longer read
-            fence_proxy_async();
-            issue<MODE, TIn>(p, maps.m, q_next, walk, smem, st);
-        }
 
         if (MODE != MODE_MERGE) {
+            // unit u inverts diagonal block u (warp 0: X00, X11; warp 1: X22, X33)
             float x[16];
-            const int b = diag_of_unit(unit);
+            const int b = unit;
             const AView a = aview<MODE, TIn>(stage, Af, b, b);
             diag_invert(a.p, a.pitch, l, x);
-            // diagonal block of the output, one lane per column
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 16; ++i) {   // diagonal block of the output, lane = column
                 const int r = 16 * b + i;
                 if (r < m.n) put1(ob + (r * os + 16 * b + l), x[i]);
             }
-            if (MODE == MODE_DIAG) {
-                float *w = p.ws + size_t(q) * 1024 + b * 256 + l;
+            if (MODE == MODE_DIAG) {         // workspace: X_bb^T row-major, lane = row
+                float4 *w = reinterpret_cast<float4 *>(p.ws + size_t(q) * 1024 + b * 256 + l * 16);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) w[i * 16] = x[i];
-                if (!L::WIDEN) {
-                    __syncthreads();
-                    if (tid == 0) {
-                        fence_proxy_async();
-                        issue<MODE, TIn>(p, maps.m, q_next, walk, smem, st);
-                    }
-                }
+                for (int i = 0; i < 4; ++i) w[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
                 continue;
             }
-            float *xs = Xs + b * XBS;
+            if (b != 3) {                    // X_bb^T row-major (row = lane)
+                float4 *d = reinterpret_cast<float4 *>(Xt + (b == 0 ? XT_00 : b == 1 ? XT_11 : XT_22) * XTS + l * XTP);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) xs[i * XP + l] = x[i];
-            __syncwarp();                    // step 0 reads only this warp's inverses
+                for (int i = 0; i < 4; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+            }
+            if (b != 0) {                    // -X_bb row-major (column = lane)
+                float *d = Xr + (b == 1 ? XR_11 : b == 3 ? XR_33 : XR_22) * XRS + l;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) d[i * XRP] = -x[i];
+            }
+            __syncwarp();                    // level A reads only this warp's inverses
         }
 
-        // ---- merge: four steps; U slots hold U' = -U
-        //   step 0  warp 0: U_A' = -X11 A10, U_B' = -X33 A32     warp 1: U00' = -X22 A20, U01' = -X22 A21
-        //   step 1  warp 0: X10 = U_A' X00, X32 = U_B' X22       warp 1: U10p' = -X33 A30, U11p' = -X33 A31
-        //   step 2  warp 0: X21 = U01' X11, X20p = U00' X00      warp 1: U10' = U10p' + (-X32) A20, U11' likewise
-        //   step 3  warp 0: X31 = U11' X11, X20 = X20p + U01' X10
-        //           warp 1: T = U10' X00 (unit 2), X30 = U11' X10 + T (unit 3)
-        float acc[4][4];
-        zero(acc);
-#pragma unroll 1
-        for (int step = 0; step < 4; ++step) {
-            const float *P;
-            const float *Q;
-            int qp = XP;
-            bool tri = false;
-            if (step == 0) {
-                tri = true;
-                if (warp == 0) {
-                    P = Xs + (half ? 3 : 1) * XBS;
-                    const AView a = aview<MODE, TIn>(stage, Af, half ? 3 : 1, half ? 2 : 0);
-                    Q = a.p; qp = a.pitch;
-                } else {
-                    P = Xs + 2 * XBS;
-                    const AView a = aview<MODE, TIn>(stage, Af, 2, half);
-                    Q = a.p; qp = a.pitch;
-                }
-            } else if (step == 1) {
-                if (warp == 0) {
-                    P = U + half * XBS;
-                    Q = Xs + (half ? 2 : 0) * XBS;
-                } else {
-                    tri = true;
-                    P = Xs + 3 * XBS;
-                    const AView a = aview<MODE, TIn>(stage, Af, 3, half);
-                    Q = a.p; qp = a.pitch;
-                }
-            } else if (step == 2) {
-                if (warp == 0) {
-                    P = U + (half ? 2 : 3) * XBS;                 // U00' : U01'
-                    Q = Xs + (half ? 0 : 1) * XBS;                // X00  : X11
-                } else {
-                    P = Xs + XS_32N * XBS;
-                    const AView a = aview<MODE, TIn>(stage, Af, 2, half);
-                    Q = a.p; qp = a.pitch;
-                }
+        // ---- level A (warp 0: X10, warp 1: X32), computed transposed:
+        //   T_A^T = X00^T A10^T,  X10^T = T_A^T (-X11)^T
+        //   T_B^T = X22^T A32^T,  X32^T = T_B^T (-X33)^T
+        {
+            TileA la;
+            TileB rb;
+            TileC c1, c2;
+            const AView a = warp == 0 ? aview<MODE, TIn>(stage, Af, 1, 0) : aview<MODE, TIn>(stage, Af, 3, 2);
+            left_smem(la, warp == 0 ? xt00 : xt22, XTP, g, t);
+            right4<AX>(rb, a.p, a.pitch, g, t);
+            zero(c1);
+            mma_tile<AX>(c1, la, rb);
+            left_regs(la, c1);
+            right2(rb, Xr + (warp == 0 ? XR_11 : XR_33) * XRS, XRP, g, t);
+            zero(c2);
+            mma_tile<false>(c2, la, rb);
+            if (warp == 0) {
+                smem_tile_t(Xt + XT_10 * XTS, c2, g, t);
+                out_tile_t(ob, os, m.n, 1, 0, c2, g, t);
             } else {
-                if (warp == 0) {
-                    P = U + (half ? 3 : 1) * XBS;                 // U01' : U11'
-                    Q = Xs + (half ? XS_10 : 1) * XBS;            // X10  : X11
-                } else {
-                    P = U + (half ? 1 : 0) * XBS;                 // U11' : U10'
-                    Q = Xs + (half ? XS_10 : 0) * XBS;            // X10  : X00
-                }
+                smem_tile_neg(Xr + XR_32 * XRS, c2, g, t);
+                out_tile_t(ob, os, m.n, 3, 2, c2, g, t);
             }
-            if (tri) prod<true>(acc, P, Q, qp, rg, cg);
-            else prod<false>(acc, P, Q, qp, rg, cg);
+        }
+        __syncthreads();
 
-            if (step == 0) {
-                put_smem<false>(U + (warp == 0 ? half : 2 + half) * XBS, acc, rg, cg);
-                zero(acc);
-                __syncthreads();
-            } else if (step == 1) {
-                if (warp == 0) {             // X10 (half 0) / X32 (half 1)
-                    if (half) put_smem<true>(Xs + XS_32N * XBS, acc, rg, cg);
-                    else put_smem<false>(Xs + XS_10 * XBS, acc, rg, cg);
-                    put_out(ob, os, m.n, half ? 3 : 1, half ? 2 : 0, acc, rg, cg);
-                    zero(acc);
-                }
-                __syncthreads();
-            } else if (step == 2) {
-                if (warp == 0) {
-                    if (!half) {             // X21 done; half 1 keeps X20p
-                        put_out(ob, os, m.n, 2, 1, acc, rg, cg);
-                        zero(acc);
-                    }
-                } else {                     // U10' / U11'
-                    put_smem<false>(U + half * XBS, acc, rg, cg);
-                    zero(acc);
-                }
-                __syncthreads();
-                if (!L::WIDEN && tid == 0) { // A is no longer read
-                    fence_proxy_async();
-                    issue<MODE, TIn>(p, maps.m, q_next, walk, smem, st);
-                }
-            } else {
-                if (warp == 0) {             // X31 (half 0) / X20 (half 1)
-                    put_out(ob, os, m.n, half ? 2 : 3, half ? 0 : 1, acc, rg, cg);
-                } else {
-                    if (!half) put_smem<false>(U + 2 * XBS, acc, rg, cg);   // T
-                    __syncwarp();
-                    if (half) {              // X30 = U11' X10 + T
-                        const float *t = U + 2 * XBS;
-#pragma unroll
-                        for (int mm = 0; mm < 4; ++mm) {
-                            const float4 v = *reinterpret_cast<const float4 *>(t + (rg + 4 * mm) * XP + 4 * cg);
-                            acc[mm][0] += v.x; acc[mm][1] += v.y; acc[mm][2] += v.z; acc[mm][3] += v.w;
-                        }
-                        put_out(ob, os, m.n, 3, 0, acc, rg, cg);
-                    }
-                }
+        // ---- level B, warp w = column block j of X_BL (w = 0: X20, X30; w = 1: X21, X31):
+        //   T_2w^T = X_TL(:, w)^T A_BL(0, :)^T,  T_3w^T = X_TL(:, w)^T A_BL(1, :)^T
+        //   X_2w^T = T_2w^T (-X22)^T,  X_3w^T = T_2w^T (-X32)^T + T_3w^T (-X33)^T
+        {
+            TileA la, lb;
+            TileB rb;
+            TileC ct2, ct3, cx;
+            zero(ct2);
+            zero(ct3);
+            left_smem(la, warp == 0 ? xt00 : xt11, XTP, g, t);   // X00^T | X11^T
+            {
+                const AView a2 = aview<MODE, TIn>(stage, Af, 2, warp), a3 = aview<MODE, TIn>(stage, Af, 3, warp);
+                right4<AX>(rb, a2.p, a2.pitch, g, t);
+                mma_tile<AX>(ct2, la, rb);
+                right4<AX>(rb, a3.p, a3.pitch, g, t);
+                mma_tile<AX>(ct3, la, rb);
             }
+            if (warp == 0) {                 // + X10^T A21^T, X10^T A31^T
+                left_smem(la, Xt + XT_10 * XTS, XTP, g, t);
+                const AView a2 = aview<MODE, TIn>(stage, Af, 2, 1), a3 = aview<MODE, TIn>(stage, Af, 3, 1);
+                right4<AX>(rb, a2.p, a2.pitch, g, t);
+                mma_tile<AX>(ct2, la, rb);
+                right4<AX>(rb, a3.p, a3.pitch, g, t);
+                mma_tile<AX>(ct3, la, rb);
+            }
+            left_regs(la, ct2);
+            left_regs(lb, ct3);
+            right2(rb, Xr + XR_22 * XRS, XRP, g, t);
+            zero(cx);
+            mma_tile<false>(cx, la, rb);
+            out_tile_t(ob, os, m.n, 2, warp, cx, g, t);
+            right2(rb, Xr + XR_32 * XRS, XRP, g, t);
+            zero(cx);
+            mma_tile<false>(cx, la, rb);
+            right2(rb, Xr + XR_33 * XRS, XRP, g, t);
+            mma_tile<false>(cx, lb, rb);
+            out_tile_t(ob, os, m.n, 3, warp, cx, g, t);
         }
     }
+    if (MODE != MODE_MERGE && tid == 0) bulk_wait_all();      // zero-block stores complete
 }
 
 }  // namespace kda
