@@ -240,7 +240,7 @@ struct Layout {
     static constexpr int WS_OFF = (A_BYTES + 127) / 128 * 128;
     static constexpr int STAGE_BYTES = MODE == MODE_MERGE ? WS_OFF + 4096 : WS_OFF;
     static constexpr uint32_t TX_BYTES = MODE == MODE_MERGE ? A_BYTES + 4096 : A_BYTES;
-    static constexpr int NAF = WIDEN ? (MODE == MODE_DIAG ? 4 : 10) : 0;   // widened A-block slots
+    static constexpr int NAF = WIDEN && MODE != MODE_MERGE ? 4 : 0;   // widened diagonal A blocks
     static constexpr int X_BYTES = MODE == MODE_DIAG ? 0 : 4 * (4 * XTS + 4 * XRS);
     static constexpr int OFF_BAR = 0;
     static constexpr int OFF_META = 64;
@@ -267,21 +267,29 @@ struct Layout {
     static constexpr int R0 = MODE == MODE_MERGE ? 1 : 0;   // first block-row fetched
 };
 
-// A-block slot of block (i, j) in the widened area
-template <int MODE>
-__device__ __forceinline__ int af_slot(int i, int j) { return MODE == MODE_DIAG ? i : blk(i, j); }
-
-// An FP32 view of A block (i, j): pointer and row pitch (floats).
+// An FP32 view of diagonal A block b: pointer and row pitch (floats).  FP32
+// input is read in place from the landing buffer; 16-bit input was widened.
 struct AView {
     const float *p;
     int pitch;
 };
 template <int MODE, typename TIn>
-__device__ __forceinline__ AView aview(const unsigned char *stage, const float *Af, int i, int j) {
+__device__ __forceinline__ AView adiag(const unsigned char *stage, const float *Af, int b) {
     using L = Layout<MODE, TIn>;
-    if (L::WIDEN) return {Af + af_slot<MODE>(i, j) * ABS, AP16};
-    const float *base = reinterpret_cast<const float *>(stage + L::row_off(i));
-    if (MODE == MODE_DIAG) return {base, 16};
+    if (L::WIDEN) return {Af + b * ABS, AP16};
+    const float *base = reinterpret_cast<const float *>(stage + L::row_off(b));
+    return {MODE == MODE_DIAG ? base : base + 16 * b, L::width(b)};
+}
+// Off-diagonal A block (i, j), i > j, in the input dtype inside the landing buffer.
+template <typename TIn>
+struct AOff {
+    const TIn *p;
+    int pitch;                 // elements
+};
+template <int MODE, typename TIn>
+__device__ __forceinline__ AOff<TIn> aoff(const unsigned char *stage, int i, int j) {
+    using L = Layout<MODE, TIn>;
+    const TIn *base = reinterpret_cast<const TIn *>(stage + L::row_off(i));
     return {base + 16 * j, L::width(i)};
 }
 
@@ -366,71 +374,41 @@ __device__ __forceinline__ void issue(const Params &p, const CUtensorMap *maps, 
 }
 
 // ------------------------------------------------------ operand preparation
-// 16-bit input: block-row R's box (16 rows x 16*NB elements from block column
-// C0) widened to FP32 tiles; rows at or past n become exact zeros (they may
-// hold the next request's rows).
-template <int MODE, typename TIn, int R, int C0, int NB>
-__device__ __forceinline__ void widen_box(const unsigned char *src, float *Af, int n, int tid) {
-    constexpr int VEC = Elt<TIn>::VEC;
-    constexpr int W = 16 * NB;
-    constexpr int VPR = W / VEC;              // vectors per row
-    constexpr int NV = 16 * VPR;
-    const bool full = n >= 16 * R + 16;
-#pragma unroll
-    for (int e0 = 0; e0 < NV; e0 += NTHREADS) {
-        const int e = e0 + tid;
-        if (NV % NTHREADS == 0 || e < NV) {
-            const int i = e / VPR;
-            const int k = (e - i * VPR) * VEC;
-            const uint4 v = *reinterpret_cast<const uint4 *>(src + (i * W + k) * int(sizeof(TIn)));
-            float f[VEC];
-            Elt<TIn>::widen(v, f);
-            const bool keep = full || (16 * R + i < n);
-            float *dst = Af + af_slot<MODE>(R, C0 + k / 16) * ABS + i * AP16 + (k & 15);
-#pragma unroll
-            for (int t = 0; t < VEC; t += 4) {
-                float4 o;
-                o.x = keep ? f[t] : 0.f;
-                o.y = keep ? f[t + 1] : 0.f;
-                o.z = keep ? f[t + 2] : 0.f;
-                o.w = keep ? f[t + 3] : 0.f;
-                *reinterpret_cast<float4 *>(dst + t) = o;
-            }
-        }
-    }
-}
-
+// 16-bit input: the four diagonal blocks widened to FP32 tiles (pitch 16);
+// rows at or past n become exact zeros (they may hold the next request's rows).
 template <int MODE, typename TIn>
-__device__ __forceinline__ void widen_all(const unsigned char *stage, float *Af, int n, int tid) {
+__device__ __forceinline__ void widen_diag(const unsigned char *stage, float *Af, int n, int tid) {
     using L = Layout<MODE, TIn>;
-    if (MODE == MODE_FUSED) {
-        widen_box<MODE, TIn, 0, 0, 1>(stage + L::row_off(0), Af, n, tid);
-        widen_box<MODE, TIn, 1, 0, 2>(stage + L::row_off(1), Af, n, tid);
-        widen_box<MODE, TIn, 2, 0, 3>(stage + L::row_off(2), Af, n, tid);
-        widen_box<MODE, TIn, 3, 0, 4>(stage + L::row_off(3), Af, n, tid);
-    } else if (MODE == MODE_DIAG) {
-        widen_box<MODE, TIn, 0, 0, 1>(stage + L::row_off(0), Af, n, tid);
-        widen_box<MODE, TIn, 1, 1, 1>(stage + L::row_off(1), Af, n, tid);
-        widen_box<MODE, TIn, 2, 2, 1>(stage + L::row_off(2), Af, n, tid);
-        widen_box<MODE, TIn, 3, 3, 1>(stage + L::row_off(3), Af, n, tid);
-    } else {
-        widen_box<MODE, TIn, 1, 0, 1>(stage + L::row_off(1), Af, n, tid);
-        widen_box<MODE, TIn, 2, 0, 2>(stage + L::row_off(2), Af, n, tid);
-        widen_box<MODE, TIn, 3, 0, 3>(stage + L::row_off(3), Af, n, tid);
+    constexpr int VEC = Elt<TIn>::VEC;       // 8 elements per 16-byte vector
+#pragma unroll
+    for (int v = 0; v < 4 * 16 * 16 / VEC / NTHREADS; ++v) {
+        const int e = tid + NTHREADS * v;    // vector index over the four blocks
+        const int b = e >> 5, i = (e >> 1) & 15, k = 8 * (e & 1);
+        const TIn *src = reinterpret_cast<const TIn *>(stage + L::row_off(b)) + i * L::width(b) +
+                         (MODE == MODE_DIAG ? 0 : 16 * b) + k;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+        float f[VEC];
+        Elt<TIn>::widen(raw, f);
+        const bool keep = 16 * b + i < n;
+        float *dst = Af + b * ABS + i * AP16 + k;
+        *reinterpret_cast<float4 *>(dst) = keep ? make_float4(f[0], f[1], f[2], f[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(dst + 4) = keep ? make_float4(f[4], f[5], f[6], f[7]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
-// FP32 input used in place: zero the rows at or past n of a partial chunk.
-template <int MODE>
+// A partial chunk: zero the rows at or past n in the landing buffer (they may
+// hold the next request's rows, and a zero times a non-finite value is not zero).
+template <int MODE, typename TIn>
 __device__ __forceinline__ void zero_rows(unsigned char *stage, int n, int tid) {
-    using L = Layout<MODE, float>;
+    using L = Layout<MODE, TIn>;
+    constexpr int VEC = 16 / int(sizeof(TIn));
 #pragma unroll
     for (int r = L::R0; r < 4; ++r) {
-        const int w4 = L::width(r) / 4;                       // float4 per row
-        float4 *base = reinterpret_cast<float4 *>(stage + L::row_off(r));
-        for (int e = tid; e < 16 * w4; e += NTHREADS) {
-            const int i = e / w4;
-            if (16 * r + i >= n) base[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int wv = L::width(r) / VEC;    // 16-byte vectors per row
+        uint4 *base = reinterpret_cast<uint4 *>(stage + L::row_off(r));
+        for (int e = tid; e < 16 * wv; e += NTHREADS) {
+            const int i = e / wv;
+            if (16 * r + i >= n) base[e] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
 }
@@ -532,6 +510,29 @@ __device__ __forceinline__ void right4(TileB &b, const float *r, int rp, int g, 
             split_tf32(v.x, b.h[0][nt][0], b.l[0][nt][0]); split_tf32(v.y, b.h[0][nt][1], b.l[0][nt][1]);
             split_tf32(v.z, b.h[1][nt][0], b.l[1][nt][0]); split_tf32(v.w, b.h[1][nt][1], b.l[1][nt][1]);
         }
+    }
+}
+
+// Right operand Q = R^T (kperm4) for a row-major A block in the input dtype.
+__device__ __forceinline__ void right4a(TileB &b, const float *r, int rp, int g, int t) {
+    right4<false>(b, r, rp, g, t);
+}
+__device__ __forceinline__ void right4a(TileB &b, const __nv_bfloat16 *r, int rp, int g, int t) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {        // bf16 -> fp32 is exact (and exact in TF32)
+        const uint2 v = *reinterpret_cast<const uint2 *>(r + (8 * nt + g) * rp + 4 * t);
+        b.h[0][nt][0] = v.x << 16; b.h[0][nt][1] = v.x & 0xffff0000u;
+        b.h[1][nt][0] = v.y << 16; b.h[1][nt][1] = v.y & 0xffff0000u;
+    }
+}
+__device__ __forceinline__ void right4a(TileB &b, const __half *r, int rp, int g, int t) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {        // fp16 -> fp32 is exact (and exact in TF32)
+        const uint2 v = *reinterpret_cast<const uint2 *>(r + (8 * nt + g) * rp + 4 * t);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+        b.h[0][nt][0] = __float_as_uint(f0.x); b.h[0][nt][1] = __float_as_uint(f0.y);
+        b.h[1][nt][0] = __float_as_uint(f1.x); b.h[1][nt][1] = __float_as_uint(f1.y);
     }
 }
 
@@ -700,12 +701,10 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             }
         }
 
-        // A operands: widened copy (16-bit input) or the landing buffer itself
-        if (L::WIDEN) {
-            widen_all<MODE, TIn>(stage, Af, m.n, tid);
-        } else if (m.n < BT) {
-            zero_rows<MODE>(stage, m.n, tid);
-        }
+        // A operands: the landing buffer itself (rows past a partial chunk's end
+        // zeroed), plus FP32 copies of the diagonal blocks for 16-bit input
+        if (m.n < BT) zero_rows<MODE, TIn>(stage, m.n, tid);
+        if (L::WIDEN && MODE != MODE_MERGE) widen_diag<MODE, TIn>(stage, Af, m.n, tid);
         // X00^T, X11^T, X22^T: the workspace tile (MODE_MERGE) or the Xt slots
         const float *xt00, *xt11, *xt22;
         if (MODE == MODE_MERGE) {
@@ -727,13 +726,13 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
         // TMA data is visible to every thread after its own mbarrier wait; a
         // barrier is needed only when threads rewrote shared memory above.
-        if (L::WIDEN || MODE == MODE_MERGE || m.n < BT) __syncthreads();
+        if ((L::WIDEN && MODE != MODE_MERGE) || MODE == MODE_MERGE || m.n < BT) __syncthreads();
 
         if (MODE != MODE_MERGE) {
             // unit u inverts diagonal block u (warp 0: X00, X11; warp 1: X22, X33)
             float x[16];
             const int b = unit;
-            const AView a = aview<MODE, TIn>(stage, Af, b, b);
+            const AView a = adiag<MODE, TIn>(stage, Af, b);
             diag_invert(a.p, a.pitch, l, x);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {   // diagonal block of the output, lane = column
@@ -766,9 +765,9 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             TileA la;
             TileB rb;
             TileC c1, c2;
-            const AView a = warp == 0 ? aview<MODE, TIn>(stage, Af, 1, 0) : aview<MODE, TIn>(stage, Af, 3, 2);
+            const AOff<TIn> a = warp == 0 ? aoff<MODE, TIn>(stage, 1, 0) : aoff<MODE, TIn>(stage, 3, 2);
             left_smem(la, warp == 0 ? xt00 : xt22, XTP, g, t);
-            right4<AX>(rb, a.p, a.pitch, g, t);
+            right4a(rb, a.p, a.pitch, g, t);
             zero(c1);
             mma_tile<AX>(c1, la, rb);
             left_regs(la, c1);
@@ -796,18 +795,18 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             zero(ct3);
             left_smem(la, warp == 0 ? xt00 : xt11, XTP, g, t);   // X00^T | X11^T
             {
-                const AView a2 = aview<MODE, TIn>(stage, Af, 2, warp), a3 = aview<MODE, TIn>(stage, Af, 3, warp);
-                right4<AX>(rb, a2.p, a2.pitch, g, t);
+                const AOff<TIn> a2 = aoff<MODE, TIn>(stage, 2, warp), a3 = aoff<MODE, TIn>(stage, 3, warp);
+                right4a(rb, a2.p, a2.pitch, g, t);
                 mma_tile<AX>(ct2, la, rb);
-                right4<AX>(rb, a3.p, a3.pitch, g, t);
+                right4a(rb, a3.p, a3.pitch, g, t);
                 mma_tile<AX>(ct3, la, rb);
             }
             if (warp == 0) {                 // + X10^T A21^T, X10^T A31^T
                 left_smem(la, Xt + XT_10 * XTS, XTP, g, t);
-                const AView a2 = aview<MODE, TIn>(stage, Af, 2, 1), a3 = aview<MODE, TIn>(stage, Af, 3, 1);
-                right4<AX>(rb, a2.p, a2.pitch, g, t);
+                const AOff<TIn> a2 = aoff<MODE, TIn>(stage, 2, 1), a3 = aoff<MODE, TIn>(stage, 3, 1);
+                right4a(rb, a2.p, a2.pitch, g, t);
                 mma_tile<AX>(ct2, la, rb);
-                right4<AX>(rb, a3.p, a3.pitch, g, t);
+                right4a(rb, a3.p, a3.pitch, g, t);
                 mma_tile<AX>(ct3, la, rb);
             }
             left_regs(la, ct2);
