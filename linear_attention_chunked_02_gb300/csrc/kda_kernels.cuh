@@ -679,11 +679,12 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         if (!m.valid) break;
         unsigned char *stage = smem + L::OFF_STAGE + st * L::STAGE_BYTES;
         const int32_t q = int32_t(blockIdx.x) + it * G;
-        // Every thread is past the previous chunk-head, so the stage it used is
-        // free: prefetch the next chunk-head into it (one iteration ahead).
+        // Every thread is past the previous chunk-head, so the stage it used,
+        // (it - 1) % STAGES, is free: refill it with the chunk-head STAGES - 1
+        // iterations ahead (the prologue issued iterations 0 .. STAGES - 1).
         if (it >= 1 && tid == 0) {
             fence_proxy_async();
-            issue<MODE, TIn>(p, maps.m, q + G, walk, smem, (it + 1) % STAGES);
+            issue<MODE, TIn>(p, maps.m, q + (STAGES - 1) * G, walk, smem, (it + STAGES - 1) % STAGES);
         }
         TOut *ob = out + (int64_t(m.row0) * p.H + m.h) * BT;      // chunk-head's first row
 
