@@ -157,11 +157,18 @@ KDA_API kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *c
 /*
  * End-to-end call for callers whose data lives in host memory: copies A (and
  * cu_seqlens) from host to the caller's device buffers, solves, and copies Ai
- * back, all enqueued on the stream; the caller synchronises the stream before
- * reading Ai_host.  Host buffers should be pinned (page-locked) for the copies
- * to be asynchronous.  A_dev / Ai_dev / cu_dev / workspace follow the rules of
- * kda_solve_tril; cu_seqlens_host and cu_dev are both NULL for the dense
- * layout.  Nothing is allocated.
+ * back.  The caller synchronises `stream` before reading Ai_host; the stream
+ * waits for the whole call.  Host buffers should be pinned (page-locked) for
+ * the copies to be asynchronous.  A_dev / Ai_dev / cu_dev / workspace follow
+ * the rules of kda_solve_tril; cu_seqlens_host and cu_dev are both NULL for
+ * the dense layout (cu_seqlens_host is read on the host).
+ *
+ * Calls moving more than 32 MiB are cut into up to 8 pieces at chunk
+ * boundaries (whole batch rows, 64-row multiples of a batch row, or whole
+ * requests); the piece copies run on two non-blocking streams that the library
+ * creates once per device and keeps until the process exits, so host-to-device
+ * copies, solves and device-to-host copies of different pieces overlap.  No
+ * device memory is allocated.
  */
 KDA_API kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, const int32_t *cu_seqlens_host,
                                  int32_t num_seqs, int64_t B, int64_t T, int32_t H,

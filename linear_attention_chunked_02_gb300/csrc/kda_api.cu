@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -131,6 +132,33 @@ kda_status_t check_args(const void *A, const void *Ai, const int32_t *cu, int32_
     return KDA_OK;
 }
 
+// Copy streams of the end-to-end entry point, created once per device.
+constexpr int kMaxPieces = 8;
+constexpr size_t kPieceBytes = size_t(16) << 20;   // at least 16 MiB of copies per piece
+struct CopyEngines {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t ev[2 + 2 * kMaxPieces] = {};
+    bool ready = false;
+};
+std::mutex g_copy_mu;
+CopyEngines g_copy[64];
+
+// With g_copy_mu held and `device` current.
+cudaError_t copy_engines(int device, CopyEngines *&ce) {
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    CopyEngines &c = g_copy[device];
+    if (!c.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
+        for (int i = 0; e == cudaSuccess && i < 2 + 2 * kMaxPieces; ++i)
+            e = cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        c.ready = true;
+    }
+    ce = &c;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -228,20 +256,95 @@ kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, const int32_
     if (st != KDA_OK) return st;
     if (B == 0 || T == 0) return KDA_OK;
     if (A_host == nullptr || Ai_host == nullptr) return KDA_ERR_INVALID_ARGUMENT;
-    const size_t elems = size_t(B) * size_t(T) * size_t(H) * kda::BT;
+    const size_t row_in = size_t(H) * kda::BT * elt_size(in_dtype);     // bytes per row of A
+    const size_t row_out = size_t(H) * kda::BT * elt_size(out_dtype);   // bytes per row of Ai
+    const int64_t rows = B * T;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(A_dev, A_host, elems * elt_size(in_dtype), cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    if (cu_dev != nullptr &&
-        cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * size_t(num_seqs + 1), cudaMemcpyHostToDevice,
-                        s) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    st = kda_solve_tril(A_dev, Ai_dev, cu_dev, num_seqs, B, T, H, in_dtype, out_dtype, workspace, workspace_bytes,
-                        stream);
-    if (st != KDA_OK) return st;
-    if (cudaMemcpyAsync(Ai_host, Ai_dev, elems * elt_size(out_dtype), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    return KDA_OK;
+
+    // Pieces cut at chunk boundaries: whole batch rows, 64-row multiples of a
+    // batch row, or whole requests; each solved as its own sub-problem.
+    struct Piece { int64_t r0, r1, b, t0, nb, nt; int32_t s0, ns; };
+    Piece pc[kMaxPieces];
+    int np = 0;
+    const size_t total = size_t(rows) * (row_in + row_out);
+    const int want = int(std::min<size_t>(kMaxPieces, std::max<size_t>(1, total / kPieceBytes)));
+    if (want > 1 && cu_dev == nullptr && B >= want) {
+        for (int k = 0; k < want; ++k) {
+            const int64_t b0 = B * k / want, b1 = B * (k + 1) / want;
+            if (b1 > b0) pc[np++] = {b0 * T, b1 * T, b0, 0, b1 - b0, T, 0, 0};
+        }
+    } else if (want > 1 && cu_dev == nullptr) {
+        const int per = std::max(1, want / int(B));                   // pieces per batch row, B * per <= want
+        const int64_t chunks = (T + kda::BT - 1) / kda::BT;
+        for (int64_t b = 0; b < B; ++b)
+            for (int k = 0; k < per; ++k) {
+                const int64_t t0 = std::min(T, chunks * k / per * kda::BT);
+                const int64_t t1 = std::min(T, chunks * (k + 1) / per * kda::BT);
+                if (t1 > t0) pc[np++] = {b * T + t0, b * T + t1, b, t0, 1, t1 - t0, 0, 0};
+            }
+    } else if (want > 1) {
+        int32_t s0 = 0;
+        for (int k = 0; k < want && s0 < num_seqs; ++k) {
+            const int64_t goal = rows * (k + 1) / want;              // rows covered after this piece
+            int32_t s1 = s0 + 1;
+            while (s1 < num_seqs && cu_seqlens_host[s1] < goal) ++s1;
+            if (k == want - 1) s1 = num_seqs;
+            pc[np++] = {cu_seqlens_host[s0], cu_seqlens_host[s1], 0, 0, 1, T, s0, s1 - s0};
+            s0 = s1;
+        }
+    }
+
+    if (np <= 1) {                           // one piece: everything on the caller's stream
+        if (cudaMemcpyAsync(A_dev, A_host, size_t(rows) * row_in, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (cu_dev != nullptr &&
+            cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * size_t(num_seqs + 1),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        st = kda_solve_tril(A_dev, Ai_dev, cu_dev, num_seqs, B, T, H, in_dtype, out_dtype, workspace,
+                            workspace_bytes, stream);
+        if (st != KDA_OK) return st;
+        if (cudaMemcpyAsync(Ai_host, Ai_dev, size_t(rows) * row_out, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        return KDA_OK;
+    }
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    CopyEngines *ce = nullptr;
+    if (copy_engines(device, ce) != cudaSuccess) return KDA_ERR_CUDA;
+    const char *ah = static_cast<const char *>(A_host);
+    char *ad = static_cast<char *>(A_dev);
+    char *oh = static_cast<char *>(Ai_host);
+    const char *od = static_cast<const char *>(Ai_dev);
+    cudaEvent_t *ev = ce->ev;                // [0] start, [1] end, then two per piece
+    bool ok = cudaEventRecord(ev[0], s) == cudaSuccess && cudaStreamWaitEvent(ce->in, ev[0], 0) == cudaSuccess &&
+              cudaStreamWaitEvent(ce->out, ev[0], 0) == cudaSuccess;
+    if (ok && cu_dev != nullptr)
+        ok = cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * size_t(num_seqs + 1),
+                             cudaMemcpyHostToDevice, ce->in) == cudaSuccess;
+    for (int k = 0; ok && k < np; ++k) {
+        const Piece &q = pc[k];
+        cudaEvent_t loaded = ev[2 + 2 * k], solved = ev[3 + 2 * k];
+        ok = cudaMemcpyAsync(ad + q.r0 * row_in, ah + q.r0 * row_in, size_t(q.r1 - q.r0) * row_in,
+                             cudaMemcpyHostToDevice, ce->in) == cudaSuccess &&
+             cudaEventRecord(loaded, ce->in) == cudaSuccess && cudaStreamWaitEvent(s, loaded, 0) == cudaSuccess;
+        if (!ok) break;
+        if (cu_dev != nullptr)               // requests s0 .. s0+ns-1, rows absolute in A
+            st = kda_solve_tril(A_dev, Ai_dev, cu_dev + q.s0, q.ns, 1, T, H, in_dtype, out_dtype, workspace,
+                                workspace_bytes, stream);
+        else
+            st = kda_solve_tril(ad + (q.b * T + q.t0) * row_in, static_cast<char *>(Ai_dev) + (q.b * T + q.t0) * row_out,
+                                nullptr, 0, q.nb, q.nt, H, in_dtype, out_dtype, workspace, workspace_bytes, stream);
+        if (st != KDA_OK) return st;
+        ok = cudaEventRecord(solved, s) == cudaSuccess && cudaStreamWaitEvent(ce->out, solved, 0) == cudaSuccess &&
+             cudaMemcpyAsync(oh + q.r0 * row_out, od + q.r0 * row_out, size_t(q.r1 - q.r0) * row_out,
+                             cudaMemcpyDeviceToHost, ce->out) == cudaSuccess;
+    }
+    // the caller's stream waits for the last copy back
+    ok = ok && cudaEventRecord(ev[1], ce->out) == cudaSuccess && cudaStreamWaitEvent(s, ev[1], 0) == cudaSuccess;
+    return ok ? KDA_OK : KDA_ERR_CUDA;
 }
 
 const char *kda_status_string(int32_t status) {

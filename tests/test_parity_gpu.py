@@ -311,6 +311,35 @@ def test_host_entry_point(kda):
     assert torch.equal(Ai_host, ref.cpu())
 
 
+HOST_PIPELINE_CASES = {
+    # > 32 MiB of copies: cut into pieces at request / batch-row / 64-row boundaries
+    "packed_16x512_f32": ki.WORKLOADS["packed_16x512_h64_f32"],
+    "packed_zero_len": ki.Workload("hp", "packed", H=64, in_dtype="f32", out_dtype="f32", seed=31,
+                                   seqlens=(0, 700, 1, 0, 2500, 64, 0, 999, 1500, 3)),
+    "dense_b1_f16": ki.Workload("hd1", "dense", H=64, in_dtype="f16", out_dtype="bf16", seed=32, B=1, T=8000),
+    "dense_b3_f32": ki.Workload("hd3", "dense", H=32, in_dtype="f32", out_dtype="f32", seed=33, B=3, T=4000),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HOST_PIPELINE_CASES))
+def test_host_entry_point_pipelined(kda, name):
+    wl = HOST_PIPELINE_CASES[name]
+    inp = ki.build(wl)
+    out_dtype = ki.torch_dtype(wl.out_dtype)
+    ref, _ = solve(kda, inp, out_dtype, "auto")
+    A, cu = to_dev(inp)
+    A_host = inp.A.pin_memory()
+    cu_host = inp.cu_seqlens.pin_memory() if cu is not None else None
+    for _ in range(2):                                   # reused copy streams and events
+        Ai_host = torch.full(inp.A.shape, float("nan"), dtype=out_dtype).pin_memory()
+        A_dev = torch.empty_like(A)
+        Ai_dev = torch.empty(inp.A.shape, dtype=out_dtype, device=DEV)
+        cu_dev = torch.empty_like(cu) if cu is not None else None
+        kda.solve_tril_host(A_host, Ai_host, A_dev, Ai_dev, cu_host, cu_dev)
+        torch.cuda.current_stream().synchronize()       # the caller's stream covers the whole call
+        assert torch.equal(Ai_host, ref.cpu()), name
+
+
 def test_no_device_error_recorded(kda):
     assert kda.device_error(0) == 0
 
