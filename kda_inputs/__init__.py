@@ -66,6 +66,7 @@ class Workload:
     seqlens: Optional[Sequence[int]] = None   # packed: fixed request lengths
     ragged: Optional[tuple] = None   # packed: (num_requests, min_len, max_len) drawn from the seed
     kind: str = "kda"                # "kda" | "nodecay" | "gauss"
+    bt: int = BT                     # chunk length (64, or the 32 / 16 branches)
 
     def with_(self, **kw) -> "Workload":
         d = dict(self.__dict__)
@@ -110,18 +111,23 @@ class SolverInput:
     def H(self) -> int:
         return self.A.shape[2]
 
+    @property
+    def bt(self) -> int:
+        return self.A.shape[3]
+
     def chunks(self):
         """(row0, n_valid) of every chunk, in order; rows index the flattened B*T axis."""
+        bt = self.bt
         out = []
         if self.cu_seqlens is None:
             for b in range(self.B):
-                for t0 in range(0, self.T, BT):
-                    out.append((b * self.T + t0, min(BT, self.T - t0)))
+                for t0 in range(0, self.T, bt):
+                    out.append((b * self.T + t0, min(bt, self.T - t0)))
         else:
             cu = self.cu_seqlens.tolist()
             for s in range(len(cu) - 1):
-                for t0 in range(cu[s], cu[s + 1], BT):
-                    out.append((t0, min(BT, cu[s + 1] - t0)))
+                for t0 in range(cu[s], cu[s + 1], bt):
+                    out.append((t0, min(bt, cu[s + 1] - t0)))
         return out
 
 
@@ -133,16 +139,16 @@ def _softplus(x: np.ndarray) -> np.ndarray:
     return np.logaddexp(0.0, x)
 
 
-def _slab(rng: np.random.Generator, L: int, H: int, kind: str) -> np.ndarray:
-    """fp64 A for one slab of L tokens: [L, H, 64], strictly lower within each chunk."""
-    C = (L + BT - 1) // BT
-    Lp = C * BT
-    row = np.arange(BT)[:, None]
-    col = np.arange(BT)[None, :]
+def _slab(rng: np.random.Generator, L: int, H: int, kind: str, bt: int = BT) -> np.ndarray:
+    """fp64 A for one slab of L tokens: [L, H, bt], strictly lower within each chunk of bt."""
+    C = (L + bt - 1) // bt
+    Lp = C * bt
+    row = np.arange(bt)[:, None]
+    col = np.arange(bt)[None, :]
     if kind == "gauss":
-        vals = rng.standard_normal((L, H, BT)) * 0.2
-        vals = np.concatenate([vals, np.zeros((Lp - L, H, BT))], axis=0)
-        S = vals.reshape(C, BT, H, BT)                       # [C, i, H, j]
+        vals = rng.standard_normal((L, H, bt)) * 0.2
+        vals = np.concatenate([vals, np.zeros((Lp - L, H, bt))], axis=0)
+        S = vals.reshape(C, bt, H, bt)                       # [C, i, H, j]
         keep = (col < row)[None, :, None, :]
     else:
         k = rng.standard_normal((L, H, KEY_DIM))
@@ -150,12 +156,12 @@ def _slab(rng: np.random.Generator, L: int, H: int, kind: str) -> np.ndarray:
         beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((L, H))))
         gpre = rng.standard_normal((L, H, KEY_DIM))
         pad = ((0, Lp - L), (0, 0), (0, 0))
-        k = np.pad(k, pad).reshape(C, BT, H, KEY_DIM)
-        beta = np.pad(beta, ((0, Lp - L), (0, 0))).reshape(C, BT, H)
+        k = np.pad(k, pad).reshape(C, bt, H, KEY_DIM)
+        beta = np.pad(beta, ((0, Lp - L), (0, 0))).reshape(C, bt, H)
         if kind == "nodecay":
             g = np.zeros_like(k)
         elif kind == "kda":
-            g = np.cumsum(-_softplus(np.pad(gpre, pad)).reshape(C, BT, H, KEY_DIM), axis=1)
+            g = np.cumsum(-_softplus(np.pad(gpre, pad)).reshape(C, bt, H, KEY_DIM), axis=1)
         else:
             raise ValueError(f"unknown input kind {kind!r}")
         # sum_d (k_i e^{g_i})_d (k_j e^{-g_j})_d, batched over chunks and heads.
@@ -165,7 +171,7 @@ def _slab(rng: np.random.Generator, L: int, H: int, kind: str) -> np.ndarray:
         S = Sc.transpose(0, 2, 1, 3) * beta[..., None]       # [C, i, H, j]
         keep = (col < row)[None, :, None, :]
     # positions past the slab end (only in the padded last chunk) are dropped below
-    A = np.where(keep, S, 0.0).reshape(Lp, H, BT)[:L]
+    A = np.where(keep, S, 0.0).reshape(Lp, H, bt)[:L]
     # a partial last chunk: columns >= n_valid are zero by construction (j < i < n_valid)
     return A
 
@@ -193,13 +199,14 @@ def build(wl: Workload, poison: bool = False) -> SolverInput:
             lens = [int(x) for x in wl.seqlens]
     else:
         raise ValueError(wl.layout)
-    slabs = [_slab(rng, L, wl.H, wl.kind) if L > 0 else np.zeros((0, wl.H, BT)) for L in lens]
+    bt = wl.bt
+    slabs = [_slab(rng, L, wl.H, wl.kind, bt) if L > 0 else np.zeros((0, wl.H, bt)) for L in lens]
     if wl.layout == "dense":
-        a = np.stack(slabs, 0) if lens else np.zeros((0, wl.T, wl.H, BT))
+        a = np.stack(slabs, 0) if lens else np.zeros((0, wl.T, wl.H, bt))
         A = _round(a, wl.in_dtype)
         cu = None
     else:
-        a = np.concatenate(slabs, 0)[None] if slabs else np.zeros((1, 0, wl.H, BT))
+        a = np.concatenate(slabs, 0)[None] if slabs else np.zeros((1, 0, wl.H, bt))
         A = _round(a, wl.in_dtype)
         cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
     out = SolverInput(wl, A.contiguous(), cu, lens)
@@ -210,10 +217,11 @@ def build(wl: Workload, poison: bool = False) -> SolverInput:
 
 def poison_ignored(inp: SolverInput) -> None:
     """Write NaN into every element of ``inp.A`` the solver is specified to ignore."""
-    flat = inp.A.view(-1, inp.H, BT)
-    col = torch.arange(BT)
+    bt = inp.bt
+    flat = inp.A.view(-1, inp.H, bt)
+    col = torch.arange(bt)
     for row0, n in inp.chunks():
         i = torch.arange(n)[:, None]
         mask = (col[None, :] >= i)                       # diagonal + upper triangle
         blk = flat[row0:row0 + n]
-        blk[mask[:, None, :].expand(n, inp.H, BT)] = float("nan")
+        blk[mask[:, None, :].expand(n, inp.H, bt)] = float("nan")

@@ -58,6 +58,11 @@ class Oracle:
         lib.kda_oracle_solve_tril.argtypes = [dp, dp, ip, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int64, ctypes.c_int32]
         lib.kda_oracle_solve_tril.restype = ctypes.c_int
+        lib.kda_oracle_invert_chunk_bt.argtypes = [dp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, dp]
+        lib.kda_oracle_invert_chunk_bt.restype = None
+        lib.kda_oracle_solve_tril_bt.argtypes = [dp, dp, ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.c_int32, ctypes.c_int32]
+        lib.kda_oracle_solve_tril_bt.restype = ctypes.c_int
         lib.kda_oracle_num_chunks.argtypes = [ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]
         lib.kda_oracle_num_chunks.restype = ctypes.c_int64
         lib.kda_oracle_num_threads.restype = ctypes.c_int
@@ -68,25 +73,26 @@ class Oracle:
     def _dptr(a: np.ndarray):
         return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
-    def invert_chunk(self, M: np.ndarray, n: Optional[int] = None) -> np.ndarray:
-        """(I + strict_lower(M[:n, :n]))^-1 embedded in a 64x64 identity, fp64."""
+    def invert_chunk(self, M: np.ndarray, n: Optional[int] = None, bt: int = BT) -> np.ndarray:
+        """(I + strict_lower(M[:n, :n]))^-1 embedded in a bt x bt identity, fp64."""
         M = np.ascontiguousarray(M, dtype=np.float64)
         if n is None:
             n = M.shape[0]
-        if M.ndim != 2 or not (0 <= n <= min(M.shape[0], M.shape[1], BT)):
-            raise ValueError(f"bad chunk shape {M.shape} for n={n}")
-        X = np.empty((BT, BT), dtype=np.float64)
-        self.lib.kda_oracle_invert_chunk(self._dptr(M), M.shape[1], int(n), self._dptr(X))
+        if M.ndim != 2 or not (0 <= n <= min(M.shape[0], M.shape[1], bt)) or not 1 <= bt <= BT:
+            raise ValueError(f"bad chunk shape {M.shape} for n={n}, bt={bt}")
+        X = np.empty((bt, bt), dtype=np.float64)
+        self.lib.kda_oracle_invert_chunk_bt(self._dptr(M), M.shape[1], int(n), int(bt), self._dptr(X))
         return X
 
     def solve_tril(self, A: np.ndarray, cu_seqlens: Optional[np.ndarray] = None) -> np.ndarray:
-        """Solve every chunk-head of A ([B, T, H, 64], any float dtype, upcast exactly).
+        """Solve every chunk-head of A ([B, T, H, bt], any float dtype, upcast exactly);
+        the chunk length bt is A's last dimension.
 
         Returns fp64 Ai of the same shape; rows that belong to no chunk are zero.
         """
         A64 = np.ascontiguousarray(A, dtype=np.float64)
-        assert A64.ndim == 4 and A64.shape[3] == BT
-        B, T, H, _ = A64.shape
+        assert A64.ndim == 4 and 1 <= A64.shape[3] <= BT
+        B, T, H, bt = A64.shape
         Ai = np.zeros_like(A64)
         if cu_seqlens is not None:
             cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
@@ -94,7 +100,7 @@ class Oracle:
             nseq = cu.shape[0] - 1
         else:
             cup, nseq = None, 0
-        rc = self.lib.kda_oracle_solve_tril(self._dptr(A64), self._dptr(Ai), cup, nseq, B, T, H)
+        rc = self.lib.kda_oracle_solve_tril_bt(self._dptr(A64), self._dptr(Ai), cup, nseq, B, T, H, bt)
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return Ai

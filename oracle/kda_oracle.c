@@ -25,6 +25,11 @@
  * batch row; packed [1, T, H, 64] with cu_seqlens restarts at every request
  * start cu_seqlens[s]; the last chunk of a row/request may be partial.
  *
+ * The same page calls this the shared solver's "64-token branch", so the
+ * chunk length is a parameter here (the _bt entry points; 16, 32 and 64 are
+ * used): the definition above is unchanged with 64 replaced by the chunk
+ * length bt.
+ *
  * Build: plain C99, -O2 -ffp-contract=off (no fused multiply-add, so the x86
  * and Arm builds give identical bits), optional -fopenmp.
  */
@@ -43,12 +48,11 @@
 #define KDA_ORACLE_PLANT 0
 #endif
 
-/* Invert one chunk.  M: row-major with leading dimension ldm; only M[i*ldm+k]
- * with k < i < n is read.  X: 64x64 row-major output (rows >= n are left
- * as identity rows, columns >= n are zero). */
-void kda_oracle_invert_chunk(const double *M, int64_t ldm, int n, double *X)
+/* Invert one chunk of length bt.  M: row-major with leading dimension ldm;
+ * only M[i*ldm+k] with k < i < n is read.  X: bt x bt row-major output (rows
+ * >= n are left as identity rows, columns >= n are zero). */
+void kda_oracle_invert_chunk_bt(const double *M, int64_t ldm, int n, int bt, double *X)
 {
-    const int bt = KDA_ORACLE_BT;
     memset(X, 0, sizeof(double) * bt * bt);
     for (int i = 0; i < bt; ++i) X[i * bt + i] = 1.0;
     for (int i = 1; i < n; ++i) {
@@ -68,16 +72,21 @@ void kda_oracle_invert_chunk(const double *M, int64_t ldm, int n, double *X)
     }
 }
 
+/* The 64-token chunk (X is 64 x 64). */
+void kda_oracle_invert_chunk(const double *M, int64_t ldm, int n, double *X)
+{
+    kda_oracle_invert_chunk_bt(M, ldm, n, KDA_ORACLE_BT, X);
+}
+
 typedef struct {
     int64_t row0;   /* first row on the flattened B*T axis */
     int n;          /* valid rows */
 } kda_oracle_chunk_t;
 
-/* Enumerate chunks; returns the count (writes up to cap entries). */
-static int64_t kda_oracle_chunks(const int32_t *cu, int32_t nseq, int64_t B, int64_t T,
+/* Enumerate chunks of length bt; returns the count (writes up to cap entries). */
+static int64_t kda_oracle_chunks(const int32_t *cu, int32_t nseq, int64_t B, int64_t T, int bt,
                                  kda_oracle_chunk_t *out, int64_t cap)
 {
-    const int bt = KDA_ORACLE_BT;
     int64_t c = 0;
     if (cu == NULL) {
         for (int64_t b = 0; b < B; ++b)
@@ -106,20 +115,20 @@ static int64_t kda_oracle_chunks(const int32_t *cu, int32_t nseq, int64_t B, int
     return c;
 }
 
-/* Solve every chunk-head.  A, Ai: fp64 [rows, H, 64] with rows = B*T, row-major,
- * contiguous.  cu_seqlens (int32 [nseq+1]) selects the packed layout (then B
- * must be 1); NULL selects the dense layout.  Rows of Ai that belong to no
- * chunk are left untouched.  Returns 0, or -1 on a bad argument. */
-int kda_oracle_solve_tril(const double *A, double *Ai, const int32_t *cu_seqlens,
-                          int32_t nseq, int64_t B, int64_t T, int32_t H)
+/* Solve every chunk-head, chunk length bt.  A, Ai: fp64 [rows, H, bt] with
+ * rows = B*T, row-major, contiguous.  cu_seqlens (int32 [nseq+1]) selects the
+ * packed layout (then B must be 1); NULL selects the dense layout.  Rows of Ai
+ * that belong to no chunk are left untouched.  Returns 0, or -1 on a bad
+ * argument. */
+int kda_oracle_solve_tril_bt(const double *A, double *Ai, const int32_t *cu_seqlens,
+                             int32_t nseq, int64_t B, int64_t T, int32_t H, int32_t bt)
 {
-    const int bt = KDA_ORACLE_BT;
-    if (H <= 0 || T < 0 || B < 0) return -1;
+    if (H <= 0 || T < 0 || B < 0 || bt < 1 || bt > 64) return -1;
     if (cu_seqlens != NULL && (B != 1 || nseq < 0)) return -1;
-    int64_t nc = kda_oracle_chunks(cu_seqlens, nseq, B, T, NULL, 0);
+    int64_t nc = kda_oracle_chunks(cu_seqlens, nseq, B, T, bt, NULL, 0);
     kda_oracle_chunk_t *ch = (kda_oracle_chunk_t *)malloc(sizeof(*ch) * (size_t)(nc > 0 ? nc : 1));
     if (!ch) return -1;
-    kda_oracle_chunks(cu_seqlens, nseq, B, T, ch, nc);
+    kda_oracle_chunks(cu_seqlens, nseq, B, T, bt, ch, nc);
     const int64_t ld = (int64_t)H * bt;          /* row stride of A / Ai in elements */
     const int64_t ntask = nc * H;
 #pragma omp parallel
@@ -130,7 +139,7 @@ int kda_oracle_solve_tril(const double *A, double *Ai, const int32_t *cu_seqlens
             const kda_oracle_chunk_t c = ch[q / H];
             const int64_t h = q % H;
             const double *M = A + c.row0 * ld + h * bt;
-            kda_oracle_invert_chunk(M, ld, c.n, X);
+            kda_oracle_invert_chunk_bt(M, ld, c.n, bt, X);
             for (int i = 0; i < c.n; ++i)
                 memcpy(Ai + (c.row0 + i) * ld + h * bt, X + i * bt, sizeof(double) * bt);
         }
@@ -140,10 +149,17 @@ int kda_oracle_solve_tril(const double *A, double *Ai, const int32_t *cu_seqlens
     return 0;
 }
 
-/* Number of chunks a layout holds (the chunk enumeration above). */
+/* The 64-token branch. */
+int kda_oracle_solve_tril(const double *A, double *Ai, const int32_t *cu_seqlens,
+                          int32_t nseq, int64_t B, int64_t T, int32_t H)
+{
+    return kda_oracle_solve_tril_bt(A, Ai, cu_seqlens, nseq, B, T, H, KDA_ORACLE_BT);
+}
+
+/* Number of 64-token chunks a layout holds (the chunk enumeration above). */
 int64_t kda_oracle_num_chunks(const int32_t *cu_seqlens, int32_t nseq, int64_t B, int64_t T)
 {
-    return kda_oracle_chunks(cu_seqlens, nseq, B, T, NULL, 0);
+    return kda_oracle_chunks(cu_seqlens, nseq, B, T, KDA_ORACLE_BT, NULL, 0);
 }
 
 /* Threads an OpenMP parallel region of this build uses (1 without OpenMP). */

@@ -278,3 +278,29 @@ def test_planted_mistake_is_caught(plant, tmp_path):
 
 def test_oracle_threads(oracle_lib):
     assert oracle_lib.num_threads() >= 1
+
+
+# ------------------------------------------- the 32- and 16-token branches
+@pytest.mark.parametrize("bt", [16, 32])
+def test_small_chunk_branches(oracle_lib, bt):
+    """Chunk length bt: nilpotent series per chunk, placement in both layouts, and
+    the hand-worked cases embedded in a bt x bt identity."""
+    orc = oracle_lib
+    for name, n, M, X in _load_golden():
+        got = orc.invert_chunk(M, n, bt=bt)
+        assert got.shape == (bt, bt)
+        assert np.array_equal(got[:n, :n], X) and np.array_equal(got[n:, n:], np.eye(bt - n)), name
+    for kind, layout in (("gauss", "packed"), ("kda", "dense"), ("nodecay", "packed")):
+        if layout == "packed":
+            wl = ki.Workload("pin", "packed", H=2, in_dtype="f32", out_dtype="f32", seed=50 + bt,
+                             seqlens=(5, 2 * bt + 3, 0, bt, 1), kind=kind, bt=bt)
+        else:
+            wl = ki.Workload("pin", "dense", H=2, in_dtype="f32", out_dtype="f32", seed=60 + bt,
+                             B=2, T=3 * bt - 5, kind=kind, bt=bt)
+        inp = ki.build(wl)
+        assert inp.A.shape[3] == bt
+        A = orc_mod.to_f64(inp.A)
+        got = orc.solve_tril(A, inp.cu_seqlens.numpy() if inp.cu_seqlens is not None else None)
+        got = got.reshape(-1, inp.H, bt)
+        want = _expected_layout(A.reshape(-1, inp.H, bt), inp.chunks(), inp.H)
+        assert np.abs(got - want).max() <= 1e-12, (kind, layout)
