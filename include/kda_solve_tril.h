@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define KDA_BT 64                 /* chunk length: the only supported size */
+#define KDA_BT 64                 /* chunk length of every entry point but kda_solve_tril_bt */
 #define KDA_WS_TILE_BYTES 4096    /* FP32 workspace per chunk-head: 4 tiles of 16x16 */
 
 typedef enum {
@@ -209,6 +209,34 @@ KDA_API kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, cons
 KDA_API kda_status_t kda_solve_tril_split_static(const void *A, void *Ai, const int32_t *cu_seqlens,
                                                  int32_t num_seqs, int64_t B, int64_t T, int32_t H,
                                                  int32_t in_dtype, int32_t out_dtype, void *stream);
+
+/*
+ * The same solve for chunks of bt = 16, 32 or 64 tokens.  The PR description
+ * names the path it optimises the shared solver's "64-token branch"; the
+ * solver's other branches invert (I + A) for the shorter chunk lengths, with A
+ * the chunk's strictly lower-triangular bt x bt block:
+ *
+ *   bt = 16  one forward substitution per chunk-head (the 16x16 diagonal
+ *            inverse on its own);
+ *   bt = 32  two 16x16 diagonal inverses and one merge step,
+ *            Linv_10 = -Linv_11 * A_10 * Linv_00, in split TF32 on the tensor
+ *            cores;
+ *   bt = 64  kda_solve_tril_ex with KDA_PATH_SINGLE (no workspace).
+ *
+ * Every argument has the meaning, layout and rules of kda_solve_tril with 64
+ * replaced by bt: A and Ai are [B, T, H, bt] (dense, chunks restart at t = 0 of
+ * each batch row) or [1, T, H, bt] with cu_seqlens (packed, chunks restart at
+ * every request start); the last chunk may hold n < bt rows; only j < i < n of
+ * a chunk's block is read; output rows of a chunk are written in full (the
+ * n x n inverse, exact ones on the diagonal, exact zeros elsewhere) and no
+ * other element of Ai is touched.  B*T < 2^31 and (chunks * H) < 2^30, counted
+ * with chunks of bt rows.  Returns KDA_ERR_UNSUPPORTED for any other bt.
+ * Accuracy: within 2e-5*(1+|ref|) of the exact inverse of the FP32-widened
+ * input on the specified workloads, as for kda_solve_tril.
+ */
+KDA_API kda_status_t kda_solve_tril_bt(const void *A, void *Ai, const int32_t *cu_seqlens,
+                                       int32_t num_seqs, int64_t B, int64_t T, int32_t H, int32_t bt,
+                                       int32_t in_dtype, int32_t out_dtype, void *stream);
 
 /* Static description of a status code (never NULL). */
 KDA_API const char *kda_status_string(int32_t status);

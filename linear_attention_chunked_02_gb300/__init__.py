@@ -2,7 +2,9 @@
 
 ``solve_tril`` computes, for every 64-token chunk and head, ``(I + A)^-1`` of
 the chunk's strictly lower-triangular matrix ``A`` (LightLLM PR #1703,
-"perf(kda): parallelize diagonal solves in Prefill").  Every step runs in the
+"perf(kda): parallelize diagonal solves in Prefill"); chunks of 16 and 32
+tokens (the solver's shorter branches) are taken from A's last dimension.
+Every step runs in the
 CUDA kernels of ``libkda_solve_tril.so``; this module only checks and
 marshals arguments (torch provides device memory and streams).
 """
@@ -16,6 +18,7 @@ import torch
 from ._lib import lib, LIB_PATH  # noqa: F401
 
 BT = 64
+CHUNK_LENGTHS = (16, 32, 64)
 WS_TILE_BYTES = 4096
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 PATH_CODE = {"auto": 0, "split": 1, "single": 2}
@@ -33,9 +36,9 @@ def _check(status: int, where: str) -> None:
         raise KdaError(status, where)
 
 
-def _shape(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor]):
-    if A.dim() != 4 or A.shape[3] != BT:
-        raise ValueError(f"A must be [B, T, H, 64], got {tuple(A.shape)}")
+def _shape(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor], lengths=(BT,)):
+    if A.dim() != 4 or A.shape[3] not in lengths:
+        raise ValueError(f"A must be [B, T, H, bt] with bt in {lengths}, got {tuple(A.shape)}")
     B, T, H, _ = A.shape
     nseq = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
     return B, T, H, nseq
@@ -62,9 +65,11 @@ def solve_tril(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
                stream: Optional[torch.cuda.Stream] = None, return_path: bool = False):
     """Per chunk-head inverse of (I + strict_lower(A)).
 
-    A: CUDA tensor [B, T, H, 64] (float32 / bfloat16 / float16), contiguous.
+    A: CUDA tensor [B, T, H, bt] (float32 / bfloat16 / float16), contiguous;
+    bt = 64, or 16 / 32 for the shorter chunk lengths.
     cu_seqlens: int32 CUDA tensor [N+1] for the packed layout (then B == 1).
-    path: "auto" (selector), "split" or "single".
+    path: "auto" (selector), "split" or "single"; chunks of 16 or 32 tokens have
+    one path only ("auto" or "single").
     workspace: optional CUDA buffer for the split path; allocated here when the
     selector would split and none is given.
     """
@@ -73,7 +78,8 @@ def solve_tril(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
     if A.dtype not in DTYPE_CODE or out_dtype not in DTYPE_CODE:
         raise ValueError(f"unsupported dtype {A.dtype} -> {out_dtype}")
     A = A.contiguous()
-    B, T, H, nseq = _shape(A, cu_seqlens)
+    B, T, H, nseq = _shape(A, cu_seqlens, CHUNK_LENGTHS)
+    bt = A.shape[3]
     if cu_seqlens is not None:
         if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
             raise ValueError("cu_seqlens must be an int32 CUDA tensor")
@@ -82,6 +88,15 @@ def solve_tril(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
         out = torch.empty(A.shape, dtype=out_dtype, device=A.device)
     elif out.shape != A.shape or out.dtype != out_dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor of A's shape and out_dtype")
+    if bt != BT:
+        if path not in ("auto", "single") or workspace is not None:
+            raise ValueError(f"{bt}-token chunks have a single path and take no workspace")
+        with torch.cuda.device(A.device):
+            st = lib().kda_solve_tril_bt(
+                A.data_ptr(), out.data_ptr(), cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+                nseq, B, T, H, bt, DTYPE_CODE[A.dtype], DTYPE_CODE[out_dtype], _stream_ptr(stream, A.device))
+        _check(st, "kda_solve_tril_bt")
+        return (out, "single") if return_path else out
     if workspace is None and path in ("auto", "split"):
         need = workspace_size(B, T, H, nseq)
         if need > 0 and (path == "split" or select_path(B, T, H, nseq, need) == "split"):

@@ -28,11 +28,11 @@ constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1 - 2 * kda::BT;
 int elt_size(int32_t dt) { return dt == KDA_F32 ? 4 : 2; }
 bool dtype_ok(int32_t dt) { return dt == KDA_F32 || dt == KDA_BF16 || dt == KDA_F16; }
 
-// Upper bound on the number of chunks that needs no look at cu_seqlens.
-int64_t max_chunks(int64_t B, int64_t T, int32_t num_seqs) {
+// Upper bound on the number of chunks of length bt that needs no look at cu_seqlens.
+int64_t max_chunks(int64_t B, int64_t T, int32_t num_seqs, int bt = kda::BT) {
     if (B <= 0 || T <= 0) return 0;
-    if (num_seqs <= 0) return B * ((T + kda::BT - 1) / kda::BT);
-    const int64_t bound = (T + int64_t(kda::BT - 1) * num_seqs) / kda::BT;
+    if (num_seqs <= 0) return B * ((T + bt - 1) / bt);
+    const int64_t bound = (T + int64_t(bt - 1) * num_seqs) / bt;
     return bound < T ? bound : T;
 }
 
@@ -120,7 +120,7 @@ cudaError_t dispatch(int mode, int32_t in_dt, int32_t out_dt, const kda::Maps &m
 
 // Host-side checks shared by every entry point.  Returns KDA_OK or an error.
 kda_status_t check_args(const void *A, const void *Ai, const int32_t *cu, int32_t num_seqs, int64_t B,
-                        int64_t T, int32_t H, int32_t in_dt, int32_t out_dt) {
+                        int64_t T, int32_t H, int32_t in_dt, int32_t out_dt, int bt = kda::BT) {
     if (!dtype_ok(in_dt) || !dtype_ok(out_dt)) return KDA_ERR_UNSUPPORTED;
     if (H < 1 || B < 0 || T < 0 || num_seqs < 0) return KDA_ERR_INVALID_ARGUMENT;
     if ((cu != nullptr) != (num_seqs > 0)) return KDA_ERR_INVALID_ARGUMENT;
@@ -128,7 +128,7 @@ kda_status_t check_args(const void *A, const void *Ai, const int32_t *cu, int32_
     if (B == 0 || T == 0) return KDA_OK;
     if (A == nullptr || Ai == nullptr) return KDA_ERR_INVALID_ARGUMENT;
     if (T > kMaxRows || B > kMaxRows / T) return KDA_ERR_UNSUPPORTED;
-    if (max_chunks(B, T, num_seqs) * H > INT32_MAX / 2) return KDA_ERR_UNSUPPORTED;
+    if (max_chunks(B, T, num_seqs, bt) * H > INT32_MAX / 2) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
 }
 
@@ -345,6 +345,42 @@ kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, const int32_
     // the caller's stream waits for the last copy back
     ok = ok && cudaEventRecord(ev[1], ce->out) == cudaSuccess && cudaStreamWaitEvent(s, ev[1], 0) == cudaSuccess;
     return ok ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_solve_tril_bt(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B,
+                               int64_t T, int32_t H, int32_t bt, int32_t in_dtype, int32_t out_dtype, void *stream) {
+    if (bt == kda::BT)
+        return kda_solve_tril_ex(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype, nullptr, 0, stream,
+                                 KDA_PATH_SINGLE, nullptr);
+    if (bt != 16 && bt != 32) return KDA_ERR_UNSUPPORTED;
+    kda_status_t st = check_args(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype, bt);
+    if (st != KDA_OK) return st;
+    if (B == 0 || T == 0) return KDA_OK;
+    const size_t elems = size_t(B) * size_t(T) * size_t(H) * size_t(bt);
+    if (!aligned16(A) || !aligned16(Ai)) return KDA_ERR_INVALID_ARGUMENT;
+    if (overlaps(A, elems * elt_size(in_dtype), Ai, elems * elt_size(out_dtype))) return KDA_ERR_INVALID_ARGUMENT;
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+    DeviceInfo info;
+    if (device_info(device, info) != cudaSuccess) return KDA_ERR_CUDA;
+    kda::SmallParams p;
+    p.A = A;
+    p.out = Ai;
+    p.cu = cu_seqlens;
+    p.nseq = num_seqs;
+    p.H = H;
+    p.T = T;
+    p.cpr = static_cast<int32_t>((T + bt - 1) / bt);
+    p.n_tasks = static_cast<int32_t>(max_chunks(B, T, num_seqs, bt) * H);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (in_dtype) {
+        case KDA_F32: e = kda::launch_small_f32(bt, out_dtype, p, device, info.num_sms, s); break;
+        case KDA_BF16: e = kda::launch_small_bf16(bt, out_dtype, p, device, info.num_sms, s); break;
+        default: e = kda::launch_small_f16(bt, out_dtype, p, device, info.num_sms, s); break;
+    }
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 const char *kda_status_string(int32_t status) {

@@ -300,12 +300,16 @@ struct Walk {
     int32_t cbase;    // chunks before request s
 };
 
+template <int CBT = BT>
 __device__ __forceinline__ int32_t nchunks(int32_t a, int32_t b) {
     const int32_t L = b - a;
-    return L > 0 ? (L + BT - 1) / BT : 0;
+    return L > 0 ? (L + CBT - 1) / CBT : 0;
 }
 
-__device__ __forceinline__ Meta decode(const Params &p, int32_t q, Walk &w) {
+// Chunk-head q -> (first row, valid rows, head) for chunk length CBT; P has the
+// layout fields cu, nseq, H, T, cpr, n_tasks.
+template <int CBT = BT, typename P>
+__device__ __forceinline__ Meta decode(const P &p, int32_t q, Walk &w) {
     Meta m{0, 0, 0, 0};
     if (q >= p.n_tasks) return m;
     const int32_t c = q / p.H;
@@ -313,23 +317,23 @@ __device__ __forceinline__ Meta decode(const Params &p, int32_t q, Walk &w) {
     if (p.cu == nullptr) {
         const int32_t b = c / p.cpr;
         const int32_t cc = c - b * p.cpr;
-        const int64_t t0 = int64_t(cc) * BT;
+        const int64_t t0 = int64_t(cc) * CBT;
         m.row0 = static_cast<int32_t>(int64_t(b) * p.T + t0);
         const int64_t left = p.T - t0;
-        m.n = static_cast<int32_t>(left < BT ? left : BT);
+        m.n = static_cast<int32_t>(left < CBT ? left : CBT);
         m.valid = 1;
         return m;
     }
-    // advance to the request that holds chunk c (tasks of a CTA increase)
+    // advance to the request that holds chunk c (tasks of a decoder increase)
     while (w.s < p.nseq) {
         const int32_t a = __ldg(p.cu + w.s), b = __ldg(p.cu + w.s + 1);
-        const int32_t nc = nchunks(a, b);
+        const int32_t nc = nchunks<CBT>(a, b);
         if (c < w.cbase + nc) {
-            int64_t r0 = int64_t(a) + int64_t(c - w.cbase) * BT;
+            int64_t r0 = int64_t(a) + int64_t(c - w.cbase) * CBT;
             int64_t end = b < p.T ? b : p.T;                  // clamp malformed cu_seqlens
             if (r0 < 0) r0 = 0;
             int64_t n = end - r0;
-            if (n > BT) n = BT;
+            if (n > CBT) n = CBT;
             if (n < 0 || r0 >= p.T) n = 0;
             m.row0 = static_cast<int32_t>(r0 < p.T ? r0 : 0);
             m.n = static_cast<int32_t>(n);

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "kda_kernels.cuh"
+#include "kda_small.cuh"
 
 namespace kda {
 
@@ -72,9 +73,64 @@ cudaError_t launch_in(int mode, int out_dtype, const Maps &maps, const Params &p
     }
 }
 
+// ------------------------------------------------ 16- and 32-token chunks
+template <int CBT, typename TIn, typename TOut>
+struct SmallKernel {
+    static constexpr int SLOTS = CBT == 16 ? 4 : 2;   // chunk-heads a CTA works on at once
+    static void (*fn())(SmallParams) { return CBT == 16 ? kda_bt16_kernel<TIn, TOut> : kda_bt32_kernel<TIn, TOut>; }
+    static int blocks_per_sm(int device, cudaError_t &err) {
+        static std::mutex mu;
+        static int cached[64] = {0};
+        std::lock_guard<std::mutex> lock(mu);
+        err = cudaSuccess;
+        if (device < 0 || device >= 64) {
+            err = cudaErrorInvalidDevice;
+            return 0;
+        }
+        if (cached[device] > 0) return cached[device];
+        int occ = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn(), NTHREADS, 0);
+        if (err != cudaSuccess) return 0;
+        cached[device] = occ > 0 ? occ : 1;
+        return cached[device];
+    }
+    static cudaError_t launch(const SmallParams &p, int device, int num_sms, cudaStream_t stream) {
+        cudaError_t err;
+        const int occ = blocks_per_sm(device, err);
+        if (err != cudaSuccess) return err;
+        long long grid = (long long)num_sms * occ;
+        const long long need = (p.n_tasks + SLOTS - 1) / SLOTS;
+        if (grid > need) grid = need;
+        if (grid < 1) return cudaSuccess;
+        fn()<<<(unsigned)grid, NTHREADS, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+};
+
+// Chunk length bt (16 or 32), dispatched on the output dtype.
+template <typename TIn>
+cudaError_t launch_small_in(int bt, int out_dtype, const SmallParams &p, int device, int num_sms,
+                            cudaStream_t stream) {
+    if (bt == 16) {
+        switch (out_dtype) {
+            case 0: return SmallKernel<16, TIn, float>::launch(p, device, num_sms, stream);
+            case 1: return SmallKernel<16, TIn, __nv_bfloat16>::launch(p, device, num_sms, stream);
+            default: return SmallKernel<16, TIn, __half>::launch(p, device, num_sms, stream);
+        }
+    }
+    switch (out_dtype) {
+        case 0: return SmallKernel<32, TIn, float>::launch(p, device, num_sms, stream);
+        case 1: return SmallKernel<32, TIn, __nv_bfloat16>::launch(p, device, num_sms, stream);
+        default: return SmallKernel<32, TIn, __half>::launch(p, device, num_sms, stream);
+    }
+}
+
 // defined in kda_inst_{f32,bf16,f16}.cu
 cudaError_t launch_f32(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
 cudaError_t launch_bf16(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
 cudaError_t launch_f16(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
+cudaError_t launch_small_f32(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
+cudaError_t launch_small_bf16(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
+cudaError_t launch_small_f16(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
 
 }  // namespace kda

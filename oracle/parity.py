@@ -40,17 +40,17 @@ def bound(ref: np.ndarray, in_dtype: torch.dtype, out_dtype: torch.dtype):
     return round_to(ref, out_dtype), tol + ulp(ref, out_dtype)
 
 
-def structure_mask(n: int) -> np.ndarray:
-    """[n, 64] True where the output is structurally fixed (diagonal, j > i, j >= n)."""
+def structure_mask(n: int, bt: int = 64) -> np.ndarray:
+    """[n, bt] True where the output is structurally fixed (diagonal, j > i, j >= n)."""
     i = np.arange(n)[:, None]
-    j = np.arange(64)[None, :]
+    j = np.arange(bt)[None, :]
     return j >= i
 
 
 def check_tile(got: np.ndarray, ref: np.ndarray, n: int, in_dtype, out_dtype):
-    """got, ref: [n, 64] of one chunk-head.  Returns (ok, max_excess, where)."""
+    """got, ref: [n, bt] of one chunk-head of chunk length bt.  Returns (ok, max_excess, where)."""
     want, tol = bound(ref, in_dtype, out_dtype)
-    st = structure_mask(n)
+    st = structure_mask(n, got.shape[1])
     if not np.array_equal(got[st], ref[st]):
         return False, float("inf"), "structure"
     diff = np.abs(got - want)

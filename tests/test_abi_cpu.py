@@ -117,3 +117,41 @@ def test_host_entry_checks(L):
     assert st == INVALID
     st = L.kda_solve_tril_host(16, 32, 48, 1, 1, 64, 1, 0, 0, 16, 1 << 20, None, None, 0, None)
     assert st == INVALID                                       # host cu without device cu
+
+
+def call_bt(L, A=16, Ai=1 << 20, cu=None, nseq=0, B=1, T=64, H=1, bt=16, ind=0, outd=0):
+    return L.kda_solve_tril_bt(A, Ai, cu, nseq, B, T, H, bt, ind, outd, None)
+
+
+def test_chunk_length_entry_checks(L):
+    for bt in (0, 8, 48, 128, -16):
+        assert call_bt(L, bt=bt) == UNSUPPORTED
+    for bt in (16, 32):
+        assert call_bt(L, bt=bt, ind=3) == UNSUPPORTED
+        assert call_bt(L, bt=bt, outd=9) == UNSUPPORTED
+        assert call_bt(L, bt=bt, H=0) == INVALID
+        assert call_bt(L, bt=bt, cu=4096, nseq=0) == INVALID
+        assert call_bt(L, bt=bt, cu=4096, nseq=1, B=2) == INVALID
+        assert call_bt(L, bt=bt, A=None) == INVALID
+        assert call_bt(L, bt=bt, Ai=(1 << 20) + 8) == INVALID      # misaligned
+        # A [1, 64, 1, bt] fp32 spans 256 bt bytes: Ai inside it overlaps
+        assert call_bt(L, bt=bt, A=1 << 20, Ai=(1 << 20) + 64 * bt * 4 - 16) == INVALID
+        assert call_bt(L, bt=bt, A=1 << 20, Ai=(1 << 20) + 64 * bt * 4) != INVALID
+        assert call_bt(L, bt=bt, T=1 << 31) == UNSUPPORTED
+        # chunks * H counted with bt-row chunks: 2^30 rows hold 2^30 / bt
+        # chunks, so bt heads reach the 2^30 chunk-head limit, bt / 2 do not
+        assert call_bt(L, bt=bt, B=1, T=1 << 30, H=bt) == UNSUPPORTED
+        assert call_bt(L, bt=bt, A=1 << 40, Ai=1 << 44, B=1, T=1 << 30, H=bt // 2) not in (UNSUPPORTED, INVALID)
+        assert call_bt(L, bt=bt, T=0) == OK
+        assert call_bt(L, bt=bt, B=0) == OK
+    # 64 goes to the single-pass 64-token path with its checks
+    assert call_bt(L, bt=64, ind=7) == UNSUPPORTED
+    assert call_bt(L, bt=64, T=0) == OK
+
+
+def test_chunk_length_entry_no_gpu(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for bt in (16, 32, 64):
+        assert call_bt(L, bt=bt, A=1 << 20, Ai=1 << 24) == CUDA

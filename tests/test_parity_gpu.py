@@ -58,13 +58,13 @@ def row_geometry(inp):
 
 def check_full(inp, got_t, ref, out_dtype, label=""):
     """Vectorised comparison of every output element against the oracle."""
-    H = inp.H
-    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, 64)
-    ref = ref.reshape(-1, H, 64)
+    H, bt = inp.H, inp.bt
+    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, bt)
+    ref = ref.reshape(-1, H, bt)
     i_in, _ = row_geometry(inp)
     covered = i_in >= 0
     got, ref, i_in = got[covered], ref[covered], i_in[covered]
-    struct = np.arange(64)[None, None, :] >= i_in[:, None, None]
+    struct = np.arange(bt)[None, None, :] >= i_in[:, None, None]
     struct = np.broadcast_to(struct, got.shape)
     assert np.array_equal(got[struct], ref[struct]), f"{label}: structural entries differ"
     assert np.all(np.isfinite(got)), f"{label}: non-finite output"
@@ -77,9 +77,9 @@ def check_full(inp, got_t, ref, out_dtype, label=""):
 
 def check_residuals(inp, got_t, out_dtype, limit=2048, seed=0):
     """||(I + M) X - I||_max per chunk-head on up to `limit` sampled chunk-heads."""
-    H = inp.H
-    A = oracle.to_f64(inp.A).reshape(-1, H, 64)
-    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, 64)
+    H, bt = inp.H, inp.bt
+    A = oracle.to_f64(inp.A).reshape(-1, H, bt)
+    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, bt)
     tasks = [(r, n, h) for (r, n) in inp.chunks() for h in range(H)]
     rng = np.random.default_rng(seed)
     if len(tasks) > limit:
@@ -372,31 +372,173 @@ def test_specified_workloads(kda, orc, name):
         outs[path] = out
     assert torch.equal(outs["single"], outs["split"])
     assert torch.equal(outs["auto"], outs["single"])
-    got = outs["auto"]
-    H = inp.H
+    check_large(orc, inp, outs["auto"], out_dtype, name)
+
+
+def check_large(orc, inp, got, out_dtype, name, full_limit=40000, samples=1024):
+    """Every element against the oracle up to `full_limit` chunk-heads; above it
+    (too large for an all-element fp64 reference) every output element's
+    structure on the device and the values of `samples` sampled chunk-heads."""
+    H, bt = inp.H, inp.bt
     ntask = len(inp.chunks()) * H
-    if ntask <= 40000:
+    if ntask <= full_limit:
         ref = oracle_ref(orc, inp)
         check_full(inp, got, ref, out_dtype, name)
     else:
-        # full size too large for an all-element fp64 reference: every output
-        # element's structure is checked on the device, values on sampled chunk-heads
-        g = got.view(-1, H, 64)
+        g = got.view(-1, H, bt)
         chunks = inp.chunks()
         i_in = torch.tensor(row_geometry(inp)[0], device=DEV)
-        j = torch.arange(64, device=DEV)
+        j = torch.arange(bt, device=DEV)
         upper = (j[None, :] > i_in[:, None])[:, None, :].expand_as(g)
         diag = (j[None, :] == i_in[:, None])[:, None, :].expand_as(g)
         assert torch.all(g[upper] == 0) and torch.all(g[diag] == 1)
         rng = np.random.default_rng(99)
-        A64 = inp.A.view(-1, H, 64)
+        Av = inp.A.view(-1, H, bt)
         gh = g.cpu()
-        for t in rng.choice(ntask, 1024, replace=False):
+        for t in rng.choice(ntask, samples, replace=False):
             row0, n = chunks[t // H]
             h = t % H
-            M = oracle.to_f64(A64[row0:row0 + n, h, :])
-            X = orc.invert_chunk(M, n)[:n, :]
+            M = oracle.to_f64(Av[row0:row0 + n, h, :])
+            X = orc.invert_chunk(M, n, bt)[:n, :]
             ok, worst, where = parity.check_tile(oracle.to_f64(gh[row0:row0 + n, h, :]), X, n,
                                                  inp.A.dtype, out_dtype)
             assert ok, (name, row0, h, where, worst)
     check_residuals(inp, got, out_dtype, limit=1024)
+
+
+# ------------------------------------------- 16- and 32-token chunk lengths
+
+SMALL_BT = [16, 32]
+SMALL_EDGE_T = [1, 2, 15, 16, 17, 31, 32, 33, 47, 48, 63, 64, 65, 100]
+NAMES = {F32: "f32", BF16: "bf16", F16: "f16"}
+
+
+@pytest.mark.parametrize("bt", SMALL_BT)
+@pytest.mark.parametrize("T", SMALL_EDGE_T)
+@pytest.mark.parametrize("H", [1, 3])
+def test_small_chunks_dense_edges(kda, orc, bt, T, H):
+    inp = ki.build(ki.Workload("edge", "dense", H=H, in_dtype="f32", out_dtype="f32", seed=T * 11 + H + bt,
+                               B=2, T=T, kind="gauss", bt=bt))
+    ref = oracle_ref(orc, inp)
+    out, taken = solve(kda, inp, F32, "auto")
+    assert taken == "single"
+    check_full(inp, out, ref, F32, f"bt={bt} T={T} H={H}")
+    check_residuals(inp, out, F32)
+
+
+@pytest.mark.parametrize("bt", SMALL_BT)
+@pytest.mark.parametrize("in_dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("out_dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("kind", ["kda", "gauss", "nodecay"])
+def test_small_chunks_dtype_matrix_packed(kda, orc, bt, in_dtype, out_dtype, kind):
+    inp = ki.build(ki.Workload("dt", "packed", H=4, in_dtype=NAMES[in_dtype], out_dtype=NAMES[out_dtype],
+                               seed=29 + bt, seqlens=(1, 15, 16, 17, 31, 32, 33, 200, 0, 7), kind=kind, bt=bt))
+    ref = oracle_ref(orc, inp)
+    out, _ = solve(kda, inp, out_dtype, "single")
+    check_full(inp, out, ref, out_dtype, f"bt={bt} {in_dtype}->{out_dtype} {kind}")
+    check_residuals(inp, out, out_dtype)
+
+
+@pytest.mark.parametrize("bt", SMALL_BT)
+@pytest.mark.parametrize("kind", ["identity", "unit_subdiag"])
+def test_small_chunks_exact_structures(kda, orc, bt, kind):
+    """A = 0 gives exactly I; A = unit subdiagonal gives exactly (-1)^(i-j) below
+    the diagonal (integers, exact in every dtype and in split TF32)."""
+    T = 3 * bt - 5
+    a = torch.zeros(1, T, 2, bt, dtype=torch.float32)
+    if kind == "unit_subdiag":
+        for r in range(T):
+            i = r % bt
+            if i > 0:
+                a[0, r, :, i - 1] = 1.0
+    for dt in DTYPES:
+        wl = ki.Workload("exact", "dense", H=2, in_dtype=NAMES[dt], out_dtype="f32", seed=0, B=1, T=T, bt=bt)
+        inp = ki.SolverInput(wl, a.to(dt).contiguous(), None, [T])
+        ref = oracle_ref(orc, inp)
+        out, _ = solve(kda, inp, F32, "single")
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref), (bt, kind, dt)
+
+
+@pytest.mark.parametrize("bt", SMALL_BT)
+def test_small_chunks_poisoned_ignored_elements(kda, bt):
+    for layout, kw in (("packed", dict(seqlens=(5, bt, 3 * bt + 1, 1, 70))), ("dense", dict(B=2, T=77))):
+        for ind in ("f32", "bf16"):
+            wl = ki.Workload("poison", layout, H=3, in_dtype=ind, out_dtype="f32", seed=23, bt=bt, **kw)
+            clean, dirty = ki.build(wl), ki.build(wl, poison=True)
+            a, _ = solve(kda, clean, F32, "single")
+            b, _ = solve(kda, dirty, F32, "single")
+            assert torch.equal(a, b), (layout, ind)
+
+
+@pytest.mark.parametrize("bt", SMALL_BT)
+@pytest.mark.parametrize("out_dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("layout", ["dense", "packed"])
+def test_small_chunks_guard_band_canaries(kda, bt, out_dtype, layout):
+    if layout == "dense":
+        wl = ki.Workload("canary", "dense", H=3, in_dtype="f32", out_dtype="f32", seed=3, B=2, T=81, bt=bt)
+    else:
+        wl = ki.Workload("canary", "packed", H=3, in_dtype="f32", out_dtype="f32", seed=3,
+                         seqlens=(7, 64, 90, 0, 1), bt=bt)
+    inp = ki.build(wl)
+    A, cu = to_dev(inp)
+    pad = 4096
+    n = A.numel()
+    buf = torch.full((pad + n + pad,), SENTINEL[out_dtype], dtype=INT_VIEW[out_dtype], device=DEV)
+    out = buf[pad:pad + n].view(out_dtype).view(A.shape)
+    kda.solve_tril(A, cu, out_dtype=out_dtype, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == SENTINEL[out_dtype]) and torch.all(buf[pad + n:] == SENTINEL[out_dtype])
+    assert not torch.any(buf[pad:pad + n] == SENTINEL[out_dtype])
+
+
+@pytest.mark.parametrize("bt", SMALL_BT)
+def test_small_chunks_packed_equals_dense_and_deterministic(kda, bt):
+    lens = (5, 64, 130, 1, 77)
+    wl = ki.Workload("pd", "packed", H=4, in_dtype="bf16", out_dtype="f32", seed=8, seqlens=lens, bt=bt)
+    inp = ki.build(wl)
+    out, _ = solve(kda, inp, F32, "single")
+    for _ in range(2):
+        again, _ = solve(kda, inp, F32, "single")
+        assert torch.equal(out, again)
+    cu = inp.cu_seqlens.tolist()
+    for s in range(len(lens)):
+        sub = inp.A[:, cu[s]:cu[s + 1]].contiguous()
+        d = ki.SolverInput(wl.with_(layout="dense", T=lens[s]), sub, None, [lens[s]])
+        o, _ = solve(kda, d, F32, "single")
+        assert torch.equal(o[0], out[0, cu[s]:cu[s + 1]]), s
+
+
+def test_small_chunks_rejected_paths(kda):
+    inp = ki.build(ki.Workload("p", "dense", H=2, in_dtype="f32", out_dtype="f32", seed=1, B=1, T=40, bt=16))
+    A, _ = to_dev(inp)
+    with pytest.raises(ValueError):
+        kda.solve_tril(A, path="split")
+    with pytest.raises(ValueError):
+        kda.solve_tril(A, workspace=torch.empty(4096, dtype=torch.uint8, device=DEV))
+    with pytest.raises(ValueError):
+        kda.solve_tril(A[..., :8].contiguous())
+
+
+def test_chunk_length_entry_64_is_single_pass(kda):
+    import ctypes
+    inp = ki.build(ki.Workload("b64", "packed", H=4, in_dtype="bf16", out_dtype="f32", seed=4,
+                               seqlens=(70, 64, 3)))
+    A, cu = to_dev(inp)
+    ref, _ = solve(kda, inp, F32, "single")
+    out = torch.empty_like(ref)
+    st = kda.lib().kda_solve_tril_bt(A.data_ptr(), out.data_ptr(), cu.data_ptr(), cu.numel() - 1, 1,
+                                     inp.T, inp.H, 64, 1, 0,
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 0 and torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("bt", SMALL_BT)
+@pytest.mark.parametrize("name", ["packed_16x512_h64_f32", "dense_8x16384_h64_f16"])
+def test_small_chunks_specified_shapes(kda, orc, bt, name):
+    """The specified workloads' shapes with bt-token chunks, every element."""
+    wl = ki.WORKLOADS[name].with_(bt=bt)
+    inp = ki.build(wl)
+    out_dtype = ki.torch_dtype(wl.out_dtype)
+    out, _ = solve(kda, inp, out_dtype, "single")
+    check_large(orc, inp, out, out_dtype, f"{name} bt={bt}", full_limit=200000)
