@@ -10,10 +10,15 @@
 //     16x16 blocks, then X10 = -X11 A10 X00 runs on the tensor cores in split
 //     TF32, computed transposed as in the 64-token kernel's level A.
 // Persistent CTAs of 64 threads walk chunk-heads q = slot, slot + slots, ...
-// Tiles are small (1-3 KiB), so loads are plain 16-byte vector loads into
-// shared memory (widened to FP32, rows past a partial chunk's end zeroed);
-// there is no asynchronous copy and no wait on a barrier other than the warp's
-// own synchronisation.
+// with one slot per unit (16 tokens) or per warp (32 tokens).  Tiles are small
+// (0.5-3 KiB), so each slot streams its own tiles through a STAGES-deep ring in
+// shared memory with cp.async: 16-byte copies, zero-fill for rows past a
+// partial chunk's end (never read), nothing for chunk-heads past the last one.
+// The next STAGES - 1 chunk-heads are in flight while one is computed.  The
+// ring holds the input bytes as they are; with 16-bit input the diagonal
+// blocks are widened once into an FP32 tile (every lane converts its share)
+// and the off-diagonal block is widened in registers by the MMA operand load.
+// Waits are cp.async.wait_group on the thread's own copies: no spin loop.
 #pragma once
 
 #include "kda_kernels.cuh"
@@ -31,95 +36,177 @@ struct SmallParams {
     int32_t n_tasks;           // loop bound on chunk-head indices
 };
 
-// Rows [r_lo, r_hi) x columns [0, w) of the chunk-head's tile (row pitch `rs`
-// elements in global memory) -> FP32 shared tile `dst` (pitch 16 per 16-column
-// block: column c goes to block c / 16).  Rows at or past n become zeros and
-// are not read.  `lanes` threads starting at lane 0 of `lane` cooperate.
+constexpr int SMALL_STAGES = 3;
+
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// 16-bit input: `nblk` 16x16 blocks of the ring (at src + 256 * blk_of(b))
+// widened into FP32 blocks dst[b] (pitch 16) by `lanes` lanes, each widening
+// 8 elements per step, so every element is converted once.
 template <typename TIn>
-__device__ __forceinline__ void load_rows(const TIn *src, int64_t rs, int r_lo, int r_hi, int w, int n,
-                                          float *dst, int blk_stride, int lane, int lanes) {
-    constexpr int VEC = Elt<TIn>::VEC;       // elements per 16-byte vector
-    const int vpr = w / VEC;
-    const int nv = (r_hi - r_lo) * vpr;
-    for (int e = lane; e < nv; e += lanes) {
-        const int i = r_lo + e / vpr;
-        const int k = (e % vpr) * VEC;
-        float f[VEC];
-        if (i < n) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(src + i * rs + k);
-            Elt<TIn>::widen(v, f);
-        } else {
-#pragma unroll
-            for (int t = 0; t < VEC; ++t) f[t] = 0.f;
-        }
-        float *d = dst + (k >> 4) * blk_stride + (i & 15) * 16 + (k & 15);
-#pragma unroll
-        for (int t = 0; t < VEC; t += 4)
-            *reinterpret_cast<float4 *>(d + t) = make_float4(f[t], f[t + 1], f[t + 2], f[t + 3]);
+__device__ __forceinline__ void widen_blocks(const TIn *src, int b_hi, float *dst, int nblk, int lane, int lanes) {
+    for (int e = lane; e < nblk * 32; e += lanes) {
+        const int b = e >> 5, o = (e & 31) * 8;
+        float f[8];
+        Elt<TIn>::widen(*reinterpret_cast<const uint4 *>(src + (b ? b_hi : 0) * 256 + o), f);
+        float4 *d = reinterpret_cast<float4 *>(dst + b * 256 + o);
+        d[0] = make_float4(f[0], f[1], f[2], f[3]);
+        d[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
 }
 
-// 16-token chunks: unit u of the CTA solves chunk-heads slot, slot + slots, ...
+// ------------------------------------------------------------ 16 tokens
+// Ring stage of one unit: the 16x16 tile, row-major, pitch 16 elements.
+template <typename TIn>
+__device__ __forceinline__ void issue16(const SmallParams &p, const Meta &m, TIn *stage, int l) {
+    constexpr int VEC = Elt<TIn>::VEC;
+    constexpr int PER_ROW = 16 / VEC;                  // 16-byte copies per row
+    if (!m.valid) return;
+    const int64_t rs = int64_t(p.H) * 16;
+    const TIn *src = reinterpret_cast<const TIn *>(p.A) + (int64_t(m.row0) * rs + int64_t(m.h) * 16);
+#pragma unroll
+    for (int e = l; e < 16 * PER_ROW; e += 16) {
+        const int i = e / PER_ROW, k = (e % PER_ROW) * VEC;
+        const bool live = i < m.n;
+        cp_async16(stage + i * 16 + k, live ? src + i * rs + k : p.A, live ? 16u : 0u);
+    }
+}
+
+// 16-token chunks: unit u of CTA b solves chunk-heads 4b + u, 4b + u + 4 grid, ...
 template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(NTHREADS, 20)
+__global__ void __launch_bounds__(NTHREADS, sizeof(TIn) == 2 ? 14 : 16)
 kda_bt16_kernel(const SmallParams p) {
-    constexpr int CBT = 16;
-    __shared__ __align__(16) float tile[4][256];
+    constexpr int S = SMALL_STAGES;
+    constexpr bool WIDEN = sizeof(TIn) == 2;
+    __shared__ __align__(16) TIn ring[4][S][256];
+    __shared__ __align__(16) float af[WIDEN ? 4 : 1][WIDEN ? 256 : 4];   // widened tile (16-bit input)
     const int tid = threadIdx.x, unit = tid >> 4, l = tid & 15;
     const unsigned mask = 0xffffu << (16 * (unit & 1));
     const int32_t slots = gridDim.x * 4;
-    const int64_t rs = int64_t(p.H) * CBT;   // row stride (elements)
+    const int32_t q0 = blockIdx.x * 4 + unit;
+    const int64_t rs = int64_t(p.H) * 16;
     Walk walk{0, 0};
-    for (int32_t q = blockIdx.x * 4 + unit;; q += slots) {
-        const Meta m = decode<CBT>(p, q, walk);
-        if (!m.valid) break;
-        const int64_t base = int64_t(m.row0) * rs + int64_t(m.h) * CBT;
-        load_rows(reinterpret_cast<const TIn *>(p.A) + base, rs, 0, 16, 16, m.n, tile[unit], 256, l, 16);
+    // metas of the chunk-heads in the ring: m[0] is computed next
+    Meta m[S];
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) {
+        m[s] = decode<16>(p, q0 + s * slots, walk);
+        issue16<TIn>(p, m[s], ring[unit][s], l);
+        cp_async_commit();
+    }
+    for (int k = 0;; ++k) {
+        m[S - 1] = decode<16>(p, q0 + (k + S - 1) * slots, walk);
+        issue16<TIn>(p, m[S - 1], ring[unit][(k + S - 1) % S], l);
+        cp_async_commit();
+        if (!m[0].valid) {                 // later chunk-heads are past the end too (nothing issued)
+            cp_async_wait<0>();
+            break;
+        }
+        cp_async_wait<S - 1>();
         __syncwarp(mask);
+        const float *a = reinterpret_cast<const float *>(ring[unit][k % S]);
+        if constexpr (WIDEN) {
+            widen_blocks(ring[unit][k % S], 0, af[unit], 1, l, 16);
+            __syncwarp(mask);
+            a = af[unit];
+        }
         float x[16];
-        diag_invert(tile[unit], 16, l, x);
-        TOut *ob = reinterpret_cast<TOut *>(p.out) + base;
+        diag_invert(a, 16, l, x);
+        TOut *ob = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * rs + int64_t(m[0].h) * 16);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            if (i < m.n) put1(ob + i * rs + l, x[i]);
-        __syncwarp(mask);                    // the tile is rewritten next
+            if (i < m[0].n) put1(ob + i * rs + l, x[i]);
+        __syncwarp(mask);                  // stage k % S is refilled next
+#pragma unroll
+        for (int s = 0; s < S - 1; ++s) m[s] = m[s + 1];
     }
 }
 
-// 32-token chunks: warp w of the CTA solves chunk-heads slot, slot + slots, ...
+// ------------------------------------------------------------ 32 tokens
+// Ring stage of one warp: blocks (0,0), (1,0), (1,1) of the chunk, each 16x16
+// row-major with pitch 16 elements, at 256-element strides.
+template <typename TIn>
+__device__ __forceinline__ void issue32(const SmallParams &p, const Meta &m, TIn *stage, int lane) {
+    constexpr int VEC = Elt<TIn>::VEC;
+    constexpr int TOP = 16 * (16 / VEC);              // copies for rows 0..15 (16 columns)
+    constexpr int ALL = TOP + 16 * (32 / VEC);        // plus rows 16..31 (32 columns)
+    if (!m.valid) return;
+    const int64_t rs = int64_t(p.H) * 32;
+    const TIn *src = reinterpret_cast<const TIn *>(p.A) + (int64_t(m.row0) * rs + int64_t(m.h) * 32);
+#pragma unroll
+    for (int e = lane; e < ALL; e += 32) {
+        int i, k;
+        if (e < TOP) {
+            i = e / (16 / VEC);
+            k = (e % (16 / VEC)) * VEC;
+        } else {
+            i = 16 + (e - TOP) / (32 / VEC);
+            k = ((e - TOP) % (32 / VEC)) * VEC;
+        }
+        const int b = i < 16 ? 0 : 1 + (k >> 4);
+        const bool live = i < m.n;
+        cp_async16(stage + b * 256 + (i & 15) * 16 + (k & 15), live ? src + i * rs + k : p.A, live ? 16u : 0u);
+    }
+}
+
+// 32-token chunks: warp w of CTA b solves chunk-heads 2b + w, 2b + w + 2 grid, ...
 template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(NTHREADS, 12)
+__global__ void __launch_bounds__(NTHREADS, 10)
 kda_bt32_kernel(const SmallParams p) {
-    constexpr int CBT = 32;
+    constexpr int S = SMALL_STAGES;
     constexpr bool AX = sizeof(TIn) == 2;    // A values exact in TF32
-    // per warp: A blocks (0,0), (1,0), (1,1) at stride 256, X00^T (pitch 16), -X11 (pitch 24)
-    __shared__ __align__(16) float ab[2][3 * 256];
-    __shared__ __align__(16) float xt[2][256];
-    __shared__ __align__(16) float xr[2][XRS];
+    __shared__ __align__(16) TIn ring[2][S][3 * 256];
+    __shared__ __align__(16) float af[2][AX ? 512 : 4];   // widened diagonal blocks (16-bit input)
+    __shared__ __align__(16) float xt[2][256];    // X00^T, pitch XTP
+    __shared__ __align__(16) float xr[2][XRS];    // -X11, pitch XRP
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = tid >> 4, half = unit & 1, l = tid & 15;
+    const int half = (tid >> 4) & 1, l = tid & 15;
     const int g = lane >> 2, t = lane & 3;
     const int32_t slots = gridDim.x * 2;
-    const int64_t rs = int64_t(p.H) * CBT;
-    const int os = p.H * CBT;
+    const int32_t q0 = blockIdx.x * 2 + warp;
+    const int os = p.H * 32;
     Walk walk{0, 0};
-    float *A0 = ab[warp];                    // block (0,0); (1,0) at +256; (1,1) at +512
-    for (int32_t q = blockIdx.x * 2 + warp;; q += slots) {
-        const Meta m = decode<CBT>(p, q, walk);
-        if (!m.valid) break;
-        const int64_t base = int64_t(m.row0) * rs + int64_t(m.h) * CBT;
-        const TIn *src = reinterpret_cast<const TIn *>(p.A) + base;
-        load_rows(src, rs, 0, 16, 16, m.n, A0, 0, lane, 32);           // block (0,0)
-        load_rows(src, rs, 16, 32, 32, m.n, A0 + 256, 256, lane, 32);  // blocks (1,0), (1,1)
+    Meta m[S];
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) {
+        m[s] = decode<32>(p, q0 + s * slots, walk);
+        issue32<TIn>(p, m[s], ring[warp][s], lane);
+        cp_async_commit();
+    }
+    for (int k = 0;; ++k) {
+        m[S - 1] = decode<32>(p, q0 + (k + S - 1) * slots, walk);
+        issue32<TIn>(p, m[S - 1], ring[warp][(k + S - 1) % S], lane);
+        cp_async_commit();
+        if (!m[0].valid) {                 // later chunk-heads are past the end too (nothing issued)
+            cp_async_wait<0>();
+            break;
+        }
+        cp_async_wait<S - 1>();
         __syncwarp();
-        TOut *ob = reinterpret_cast<TOut *>(p.out) + base;
+        const TIn *a = ring[warp][k % S];
+        const int n = m[0].n;
+        TOut *ob = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * os + int64_t(m[0].h) * 32);
         {
+            const float *d = reinterpret_cast<const float *>(a) + (half ? 512 : 0);
+            if constexpr (AX) {              // blocks (0,0) and (1,1)
+                widen_blocks(a, 2, af[warp], 2, lane, 32);
+                __syncwarp();
+                d = af[warp] + (half ? 256 : 0);
+            }
             float x[16];
-            diag_invert(A0 + (half ? 512 : 0), 16, l, x);
+            diag_invert(d, 16, l, x);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {   // diagonal block of the output, lane = column
                 const int r = 16 * half + i;
-                if (r < m.n) put1(ob + (r * os + 16 * half + l), x[i]);
+                if (r < n) put1(ob + (r * os + 16 * half + l), x[i]);
             }
             if (!half) {                     // X00^T row-major (row = lane)
                 float4 *d = reinterpret_cast<float4 *>(xt[warp] + l * XTP);
@@ -130,13 +217,12 @@ kda_bt32_kernel(const SmallParams p) {
                 for (int i = 0; i < 16; ++i) xr[warp][i * XRP + l] = -x[i];
             }
         }
-        // zero block (0,1): rows 0..15 below n, columns 16..31
-        {
+        {                                    // zero block (0,1): rows 0..15 below n, columns 16..31
             constexpr int VEC = 16 / int(sizeof(TOut));
 #pragma unroll
             for (int e = lane; e < 16 * (16 / VEC); e += 32) {
                 const int r = e / (16 / VEC), c = 16 + VEC * (e % (16 / VEC));
-                if (r < m.n) *reinterpret_cast<uint4 *>(ob + (r * os + c)) = make_uint4(0u, 0u, 0u, 0u);
+                if (r < n) *reinterpret_cast<uint4 *>(ob + (r * os + c)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         __syncwarp();
@@ -145,15 +231,17 @@ kda_bt32_kernel(const SmallParams p) {
         TileB rb;
         TileC c1, c2;
         left_smem(la, xt[warp], XTP, g, t);
-        right4<AX>(rb, A0 + 256, 16, g, t);
+        right4a(rb, a + 256, 16, g, t);
         zero(c1);
         mma_tile<AX>(c1, la, rb);
         left_regs(la, c1);
         right2(rb, xr[warp], XRP, g, t);
         zero(c2);
         mma_tile<false>(c2, la, rb);
-        out_tile_t(ob, os, m.n, 1, 0, c2, g, t);
-        __syncwarp();                        // the tiles are rewritten next
+        out_tile_t(ob, os, n, 1, 0, c2, g, t);
+        __syncwarp();                        // xt, xr and stage k % S are rewritten next
+#pragma unroll
+        for (int s = 0; s < S - 1; ++s) m[s] = m[s + 1];
     }
 }
 
