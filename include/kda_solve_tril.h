@@ -126,7 +126,8 @@ KDA_API kda_path_t kda_solve_tril_select(int64_t B, int64_t T, int32_t H, int32_
  *               results but every access stays inside rows [0, T).
  *   num_seqs    number of requests (packed) or 0 (dense).
  *   B, T, H     shape; T == 0 or B == 0 is a no-op returning KDA_OK.  H >= 1,
- *               B*T < 2^31 and (chunks * H) < 2^30.
+ *               H * 64 * 64 < 2^31 (H < 524288), B*T < 2^31 and
+ *               (chunks * H) < 2^30; larger sizes give KDA_ERR_UNSUPPORTED.
  *   in_dtype    KDA_F32 / KDA_BF16 / KDA_F16; values are widened to FP32.
  *   out_dtype   KDA_F32 / KDA_BF16 / KDA_F16; FP32 results rounded to nearest even.
  *   workspace   device, 16-byte aligned, or NULL; used only by the split path.
@@ -229,8 +230,9 @@ KDA_API kda_status_t kda_solve_tril_split_static(const void *A, void *Ai, const 
  * every request start); the last chunk may hold n < bt rows; only j < i < n of
  * a chunk's block is read; output rows of a chunk are written in full (the
  * n x n inverse, exact ones on the diagonal, exact zeros elsewhere) and no
- * other element of Ai is touched.  B*T < 2^31 and (chunks * H) < 2^30, counted
- * with chunks of bt rows.  Returns KDA_ERR_UNSUPPORTED for any other bt.
+ * other element of Ai is touched.  H * bt * bt < 2^31, B*T < 2^31 and
+ * (chunks * H) < 2^30, counted with chunks of bt rows.  Returns
+ * KDA_ERR_UNSUPPORTED for any other bt.
  * Accuracy: within 2e-5*(1+|ref|) of the exact inverse of the FP32-widened
  * input on the specified workloads, as for kda_solve_tril.
  */

@@ -123,6 +123,7 @@ kda_status_t check_args(const void *A, const void *Ai, const int32_t *cu, int32_
                         int64_t T, int32_t H, int32_t in_dt, int32_t out_dt, int bt = kda::BT) {
     if (!dtype_ok(in_dt) || !dtype_ok(out_dt)) return KDA_ERR_UNSUPPORTED;
     if (H < 1 || B < 0 || T < 0 || num_seqs < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (int64_t(H) * bt * bt > INT32_MAX) return KDA_ERR_UNSUPPORTED;   // in-chunk offsets are 32-bit
     if ((cu != nullptr) != (num_seqs > 0)) return KDA_ERR_INVALID_ARGUMENT;
     if (cu != nullptr && B != 1) return KDA_ERR_INVALID_ARGUMENT;
     if (B == 0 || T == 0) return KDA_OK;

@@ -306,14 +306,12 @@ __device__ __forceinline__ int32_t nchunks(int32_t a, int32_t b) {
     return L > 0 ? (L + CBT - 1) / CBT : 0;
 }
 
-// Chunk-head q -> (first row, valid rows, head) for chunk length CBT; P has the
-// layout fields cu, nseq, H, T, cpr, n_tasks.
+// Chunk c, head h -> (first row, valid rows, head) for chunk length CBT; P has
+// the layout fields cu, nseq, T, cpr.  Packed: w walks cu_seqlens forward, so
+// the chunks a walker locates must not decrease.
 template <int CBT = BT, typename P>
-__device__ __forceinline__ Meta decode(const P &p, int32_t q, Walk &w) {
-    Meta m{0, 0, 0, 0};
-    if (q >= p.n_tasks) return m;
-    const int32_t c = q / p.H;
-    m.h = q - c * p.H;
+__device__ __forceinline__ Meta locate(const P &p, int32_t c, int32_t h, Walk &w) {
+    Meta m{0, 0, h, 0};
     if (p.cu == nullptr) {
         const int32_t b = c / p.cpr;
         const int32_t cc = c - b * p.cpr;
@@ -324,7 +322,7 @@ __device__ __forceinline__ Meta decode(const P &p, int32_t q, Walk &w) {
         m.valid = 1;
         return m;
     }
-    // advance to the request that holds chunk c (tasks of a decoder increase)
+    // advance to the request that holds chunk c
     while (w.s < p.nseq) {
         const int32_t a = __ldg(p.cu + w.s), b = __ldg(p.cu + w.s + 1);
         const int32_t nc = nchunks<CBT>(a, b);
@@ -344,6 +342,15 @@ __device__ __forceinline__ Meta decode(const P &p, int32_t q, Walk &w) {
         ++w.s;
     }
     return m;
+}
+
+// Chunk-head q -> (first row, valid rows, head) for chunk length CBT; P has the
+// layout fields cu, nseq, H, T, cpr, n_tasks.  Tasks of one walker increase.
+template <int CBT = BT, typename P>
+__device__ __forceinline__ Meta decode(const P &p, int32_t q, Walk &w) {
+    if (q >= p.n_tasks) return Meta{0, 0, 0, 0};
+    const int32_t c = q / p.H;
+    return locate<CBT>(p, c, q - c * p.H, w);
 }
 
 // Issue the loads of task q into stage `st` (one thread).
@@ -566,9 +573,9 @@ __device__ __forceinline__ void mma_tile(TileC &c, const TileA &a, const TileB &
 }
 
 // C tile holding Y^T -> output block (bi, bj) of the chunk (rows below n only).
-template <typename TOut>
+template <int CBT = BT, typename TOut>
 __device__ __forceinline__ void out_tile_t(TOut *ob, int os, int n, int bi, int bj, const TileC &c, int g, int t) {
-    const bool full = n == BT;
+    const bool full = n == CBT;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll

@@ -38,6 +38,33 @@ struct SmallParams {
 
 constexpr int SMALL_STAGES = 3;
 
+// Chunk-heads q = q0, q0 + step, ... of one slot; chunk c = q / H and head
+// h = q % H are advanced incrementally (one division at the start).
+template <int CBT>
+struct SlotWalk {
+    int32_t q, c, h, step, sc, sh;
+    Walk w;
+    __device__ __forceinline__ SlotWalk(const SmallParams &p, int32_t q0, int32_t step_)
+        : q(q0), step(step_), w{0, 0} {
+        c = q0 / p.H;
+        h = q0 - c * p.H;
+        sc = step_ / p.H;
+        sh = step_ - sc * p.H;
+    }
+    // meta of the current chunk-head, then advance to the next
+    __device__ __forceinline__ Meta next(const SmallParams &p) {
+        const Meta m = q < p.n_tasks ? locate<CBT>(p, c, h, w) : Meta{0, 0, 0, 0};
+        q += step;
+        c += sc;
+        h += sh;
+        if (h >= p.H) {
+            h -= p.H;
+            ++c;
+        }
+        return m;
+    }
+};
+
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
@@ -64,19 +91,23 @@ __device__ __forceinline__ void widen_blocks(const TIn *src, int b_hi, float *ds
 }
 
 // ------------------------------------------------------------ 16 tokens
-// Ring stage of one unit: the 16x16 tile, row-major, pitch 16 elements.
+// Ring stage of one unit: the 16x16 tile, row-major, pitch 16 elements.  Lane
+// l copies 16 bytes of rows i0, i0 + DI, ... (i0 = l / PER_ROW).
 template <typename TIn>
 __device__ __forceinline__ void issue16(const SmallParams &p, const Meta &m, TIn *stage, int l) {
     constexpr int VEC = Elt<TIn>::VEC;
     constexpr int PER_ROW = 16 / VEC;                  // 16-byte copies per row
+    constexpr int DI = 16 / PER_ROW;                   // rows between a lane's copies
     if (!m.valid) return;
-    const int64_t rs = int64_t(p.H) * 16;
-    const TIn *src = reinterpret_cast<const TIn *>(p.A) + (int64_t(m.row0) * rs + int64_t(m.h) * 16);
+    const int rs = p.H * 16;                           // row stride (elements)
+    const int i0 = l / PER_ROW, k = (l % PER_ROW) * VEC;
+    const TIn *src = reinterpret_cast<const TIn *>(p.A) + (int64_t(m.row0) * rs + m.h * 16) + (i0 * rs + k);
+    TIn *dst = stage + i0 * 16 + k;
 #pragma unroll
-    for (int e = l; e < 16 * PER_ROW; e += 16) {
-        const int i = e / PER_ROW, k = (e % PER_ROW) * VEC;
-        const bool live = i < m.n;
-        cp_async16(stage + i * 16 + k, live ? src + i * rs + k : p.A, live ? 16u : 0u);
+    for (int it = 0; it < PER_ROW; ++it) {
+        const bool live = i0 + DI * it < m.n;
+        cp_async16(dst + DI * 16 * it, live ? src : p.A, live ? 16u : 0u);
+        src += DI * rs;
     }
 }
 
@@ -92,18 +123,18 @@ kda_bt16_kernel(const SmallParams p) {
     const unsigned mask = 0xffffu << (16 * (unit & 1));
     const int32_t slots = gridDim.x * 4;
     const int32_t q0 = blockIdx.x * 4 + unit;
-    const int64_t rs = int64_t(p.H) * 16;
-    Walk walk{0, 0};
+    const int rs = p.H * 16;                 // row stride (elements); H * 16 * 16 < 2^31
+    SlotWalk<16> walk(p, q0, slots);
     // metas of the chunk-heads in the ring: m[0] is computed next
     Meta m[S];
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
-        m[s] = decode<16>(p, q0 + s * slots, walk);
+        m[s] = walk.next(p);
         issue16<TIn>(p, m[s], ring[unit][s], l);
         cp_async_commit();
     }
     for (int k = 0;; ++k) {
-        m[S - 1] = decode<16>(p, q0 + (k + S - 1) * slots, walk);
+        m[S - 1] = walk.next(p);
         issue16<TIn>(p, m[S - 1], ring[unit][(k + S - 1) % S], l);
         cp_async_commit();
         if (!m[0].valid) {                 // later chunk-heads are past the end too (nothing issued)
@@ -120,10 +151,15 @@ kda_bt16_kernel(const SmallParams p) {
         }
         float x[16];
         diag_invert(a, 16, l, x);
-        TOut *ob = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * rs + int64_t(m[0].h) * 16);
+        TOut *op = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * rs + (m[0].h * 16 + l));
+        if (m[0].n == 16) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (i < m[0].n) put1(ob + i * rs + l, x[i]);
+            for (int i = 0; i < 16; ++i, op += rs) put1(op, x[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i, op += rs)
+                if (i < m[0].n) put1(op, x[i]);
+        }
         __syncwarp(mask);                  // stage k % S is refilled next
 #pragma unroll
         for (int s = 0; s < S - 1; ++s) m[s] = m[s + 1];
@@ -132,28 +168,37 @@ kda_bt16_kernel(const SmallParams p) {
 
 // ------------------------------------------------------------ 32 tokens
 // Ring stage of one warp: blocks (0,0), (1,0), (1,1) of the chunk, each 16x16
-// row-major with pitch 16 elements, at 256-element strides.
+// row-major with pitch 16 elements, at 256-element strides.  Rows 0..15 need
+// 16 columns, rows 16..31 all 32: lane l copies 16 bytes of top rows i0,
+// i0 + DT, ... and of bottom rows 16 + j0, 16 + j0 + DB, ...
 template <typename TIn>
 __device__ __forceinline__ void issue32(const SmallParams &p, const Meta &m, TIn *stage, int lane) {
     constexpr int VEC = Elt<TIn>::VEC;
-    constexpr int TOP = 16 * (16 / VEC);              // copies for rows 0..15 (16 columns)
-    constexpr int ALL = TOP + 16 * (32 / VEC);        // plus rows 16..31 (32 columns)
+    constexpr int PT = 16 / VEC, PB = 32 / VEC;        // 16-byte copies per top / bottom row
+    constexpr int DT = 32 / PT, DB = 32 / PB;          // rows between a lane's copies
     if (!m.valid) return;
-    const int64_t rs = int64_t(p.H) * 32;
-    const TIn *src = reinterpret_cast<const TIn *>(p.A) + (int64_t(m.row0) * rs + int64_t(m.h) * 32);
+    const int rs = p.H * 32;
+    const TIn *base = reinterpret_cast<const TIn *>(p.A) + (int64_t(m.row0) * rs + m.h * 32);
+    {
+        const int i0 = lane / PT, k = (lane % PT) * VEC;
+        const TIn *src = base + (i0 * rs + k);
 #pragma unroll
-    for (int e = lane; e < ALL; e += 32) {
-        int i, k;
-        if (e < TOP) {
-            i = e / (16 / VEC);
-            k = (e % (16 / VEC)) * VEC;
-        } else {
-            i = 16 + (e - TOP) / (32 / VEC);
-            k = ((e - TOP) % (32 / VEC)) * VEC;
+        for (int it = 0; it < 16 / DT; ++it) {
+            const bool live = i0 + DT * it < m.n;
+            cp_async16(stage + (i0 + DT * it) * 16 + k, live ? src : p.A, live ? 16u : 0u);
+            src += DT * rs;
         }
-        const int b = i < 16 ? 0 : 1 + (k >> 4);
-        const bool live = i < m.n;
-        cp_async16(stage + b * 256 + (i & 15) * 16 + (k & 15), live ? src + i * rs + k : p.A, live ? 16u : 0u);
+    }
+    {
+        const int j0 = lane / PB, k = (lane % PB) * VEC;
+        const TIn *src = base + ((16 + j0) * rs + k);
+        TIn *dst = stage + (1 + (k >> 4)) * 256 + j0 * 16 + (k & 15);
+#pragma unroll
+        for (int it = 0; it < 16 / DB; ++it) {
+            const bool live = 16 + j0 + DB * it < m.n;
+            cp_async16(dst + DB * 16 * it, live ? src : p.A, live ? 16u : 0u);
+            src += DB * rs;
+        }
     }
 }
 
@@ -173,16 +218,16 @@ kda_bt32_kernel(const SmallParams p) {
     const int32_t slots = gridDim.x * 2;
     const int32_t q0 = blockIdx.x * 2 + warp;
     const int os = p.H * 32;
-    Walk walk{0, 0};
+    SlotWalk<32> walk(p, q0, slots);
     Meta m[S];
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
-        m[s] = decode<32>(p, q0 + s * slots, walk);
+        m[s] = walk.next(p);
         issue32<TIn>(p, m[s], ring[warp][s], lane);
         cp_async_commit();
     }
     for (int k = 0;; ++k) {
-        m[S - 1] = decode<32>(p, q0 + (k + S - 1) * slots, walk);
+        m[S - 1] = walk.next(p);
         issue32<TIn>(p, m[S - 1], ring[warp][(k + S - 1) % S], lane);
         cp_async_commit();
         if (!m[0].valid) {                 // later chunk-heads are past the end too (nothing issued)
@@ -193,7 +238,7 @@ kda_bt32_kernel(const SmallParams p) {
         __syncwarp();
         const TIn *a = ring[warp][k % S];
         const int n = m[0].n;
-        TOut *ob = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * os + int64_t(m[0].h) * 32);
+        TOut *ob = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * os + m[0].h * 32);
         {
             const float *d = reinterpret_cast<const float *>(a) + (half ? 512 : 0);
             if constexpr (AX) {              // blocks (0,0) and (1,1)
@@ -203,10 +248,14 @@ kda_bt32_kernel(const SmallParams p) {
             }
             float x[16];
             diag_invert(d, 16, l, x);
+            TOut *op = ob + (16 * half * os + 16 * half + l);   // diagonal block, lane = column
+            if (n == 32) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {   // diagonal block of the output, lane = column
-                const int r = 16 * half + i;
-                if (r < n) put1(ob + (r * os + 16 * half + l), x[i]);
+                for (int i = 0; i < 16; ++i, op += os) put1(op, x[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i, op += os)
+                    if (16 * half + i < n) put1(op, x[i]);
             }
             if (!half) {                     // X00^T row-major (row = lane)
                 float4 *d = reinterpret_cast<float4 *>(xt[warp] + l * XTP);
@@ -238,7 +287,7 @@ kda_bt32_kernel(const SmallParams p) {
         right2(rb, xr[warp], XRP, g, t);
         zero(c2);
         mma_tile<false>(c2, la, rb);
-        out_tile_t(ob, os, n, 1, 0, c2, g, t);
+        out_tile_t<32>(ob, os, n, 1, 0, c2, g, t);
         __syncwarp();                        // xt, xr and stage k % S are rewritten next
 #pragma unroll
         for (int s = 0; s < S - 1; ++s) m[s] = m[s + 1];

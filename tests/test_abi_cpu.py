@@ -87,6 +87,8 @@ def test_argument_errors_before_any_cuda_call(L):
     assert call(L, A=1 << 20, Ai=(1 << 20) + 4096)[0] == INVALID   # overlapping
     assert call(L, path=5)[0] == INVALID
     assert call(L, T=1 << 31)[0] == UNSUPPORTED
+    assert call(L, H=1 << 19)[0] == UNSUPPORTED                # H * 64 * 64 >= 2^31
+    assert call(L, A=1 << 40, Ai=1 << 44, H=(1 << 19) - 1)[0] != UNSUPPORTED
     assert call(L, path=1, ws=None)[0] == WORKSPACE            # forced split, no workspace
     assert call(L, path=1, ws=1 << 24, wsb=100)[0] == WORKSPACE
     assert call(L, path=1, ws=(1 << 24) + 8, wsb=1 << 20)[0] == INVALID  # misaligned workspace
@@ -138,6 +140,7 @@ def test_chunk_length_entry_checks(L):
         assert call_bt(L, bt=bt, A=1 << 20, Ai=(1 << 20) + 64 * bt * 4 - 16) == INVALID
         assert call_bt(L, bt=bt, A=1 << 20, Ai=(1 << 20) + 64 * bt * 4) != INVALID
         assert call_bt(L, bt=bt, T=1 << 31) == UNSUPPORTED
+        assert call_bt(L, bt=bt, H=(1 << 31) // (bt * bt)) == UNSUPPORTED   # H * bt * bt >= 2^31
         # chunks * H counted with bt-row chunks: 2^30 rows hold 2^30 / bt
         # chunks, so bt heads reach the 2^30 chunk-head limit, bt / 2 do not
         assert call_bt(L, bt=bt, B=1, T=1 << 30, H=bt) == UNSUPPORTED
