@@ -7,6 +7,9 @@ path also the workspace round trip) on the packed workload of 16 requests x
 metric is quoted on).  Inputs are synthetic (seeded KDA-style A).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--bt 16|32|64]
+
+``--bt`` times the solver's 16- or 32-token branch on the workload's shape.
 
 Prints one JSON line (rank 0).  N > 1 runs one independent replica per GPU
 (no collective on the data path); the value is the sum over ranks.
@@ -34,6 +37,8 @@ import kda_inputs as ki  # noqa: E402
 METRIC = "solve ms & achieved HBM GB/s (vs ~8 TB/s) at 8192 tok x 64 heads, 1 GB300"
 WORKLOAD = "packed_16x512_h64_f32"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 10 ** 6
+KERNEL = {64: "kda_tril_kernel<MODE_FUSED>", 32: "kda_bt32_kernel", 16: "kda_bt16_kernel"}
 DTYPE_NAME = {"f32": "f32", "bf16": "bf16", "f16": "f16"}
 ELT = {"f32": 4, "bf16": 2, "f16": 2}
 
@@ -51,7 +56,7 @@ def algorithmic_bytes(inp: ki.SolverInput, in_elt: int, out_elt: int) -> int:
     tot = 0
     for _, n in inp.chunks():
         if n not in per_n:
-            per_n[n] = sector_read_bytes(n, in_elt) + n * 64 * out_elt
+            per_n[n] = sector_read_bytes(n, in_elt) + n * inp.bt * out_elt
         tot += per_n[n]
     return tot * inp.H
 
@@ -131,27 +136,77 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# sources that define each kernel family and its launch
+_COMMON_SOURCES = ["kda_kernels.cuh", "kda_launch.cuh", "kda_api.cu", "kda_inst_f32.cu",
+                   "kda_inst_bf16.cu", "kda_inst_f16.cu"]
+KERNEL_SOURCES = {"kda_tril_kernel": _COMMON_SOURCES, "kda_bt": _COMMON_SOURCES + ["kda_small.cuh"]}
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_source_hash(kernel: str) -> str:
+    files = next(v for k, v in KERNEL_SOURCES.items() if kernel.startswith(k))
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_chunked_02_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def flushes_l2(inp: ki.SolverInput) -> bool:
+    """Footprints under twice the L2 are timed step by step with an L2 flush between."""
+    wl = inp.workload
+    return full_tensor_bytes(inp, ELT[wl.in_dtype], ELT[wl.out_dtype]) < 2 * L2_BYTES
+
+
+def workload_key(wl: ki.Workload) -> str:
+    return wl.name if wl.bt == 64 else f"{wl.name}_bt{wl.bt}"
 
 
 def ncu_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was
     taken on the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        d = json.load(open(p))
+        d = json.load(open(TRAFFIC_JSON))
     except (OSError, ValueError):
         return None
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
+
+
+_UNIT = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+
+
+def record_traffic(csv_path: str, workload: str, kernel: str, command: str) -> dict:
+    """Store the DRAM bytes of the one captured launch in an ncu --csv log (metrics
+    dram__bytes_read.sum and dram__bytes_write.sum) under (workload, kernel)."""
+    import csv
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    vals = {}
+    for r in csv.DictReader(lines):
+        name = r.get("Metric Name")
+        if name in ("dram__bytes_read.sum", "dram__bytes_write.sum", "gpu__time_duration.sum"):
+            v = float(r["Metric Value"].replace(",", ""))
+            vals.setdefault(r["ID"], {})[name] = v * _UNIT.get(r.get("Metric Unit", "byte"), 1.0)
+    if len(vals) != 1:
+        raise ValueError(f"expected one captured launch in {csv_path}, found {len(vals)}")
+    m = next(iter(vals.values()))
+    entry = {"source_hash": kernel_source_hash(kernel),
+             "dram_bytes_per_launch": int(m["dram__bytes_read.sum"] + m["dram__bytes_write.sum"]),
+             "dram_read": int(m["dram__bytes_read.sum"]), "dram_write": int(m["dram__bytes_write.sum"]),
+             "note": f"one ncu launch capture: {command}; output lines still dirty in L2 at kernel "
+                     "end are not in the write figure"}
+    try:
+        d = json.load(open(TRAFFIC_JSON))
+    except (OSError, ValueError):
+        d = {}
+    d.setdefault(workload, {})[kernel] = entry
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(d, f, indent=1)
+        f.write("\n")
+    return entry
 
 
 # ------------------------------------------------------------------ ranks
@@ -209,7 +264,7 @@ def run_reference(args, world, rank):
     """The oracle, as it stands, on the host cores: the reference arm."""
     if rank != 0:
         return
-    wl = ki.WORKLOADS[args.workload]
+    wl = ki.WORKLOADS[args.workload].with_(bt=args.bt)
     inp = ki.build(wl)
     ine, oute = ELT[wl.in_dtype], ELT[wl.out_dtype]
     alg = algorithmic_bytes(inp, ine, oute)
@@ -240,11 +295,12 @@ def run_reference(args, world, rank):
 
 def config_dict(inp: ki.SolverInput, path: str):
     wl = inp.workload
-    return {"workload": wl.name, "layout": wl.layout, "tokens": inp.B * inp.T,
-            "requests": len(inp.seqlens), "heads": inp.H, "in_dtype": wl.in_dtype,
-            "out_dtype": wl.out_dtype, "path": path,
-            "l2": "input+output %.0f MB > 129 MB L2; no flush between steps"
-                  % (full_tensor_bytes(inp, ELT[wl.in_dtype], ELT[wl.out_dtype]) / 1e6)}
+    mb = full_tensor_bytes(inp, ELT[wl.in_dtype], ELT[wl.out_dtype]) / 1e6
+    l2 = (f"input+output {mb:.0f} MB < 2 x 129 MB L2: 256 MB written between steps, each step timed alone"
+          if flushes_l2(inp) else f"input+output {mb:.0f} MB > 129 MB L2; no flush between steps")
+    return {"workload": workload_key(wl), "layout": wl.layout, "tokens": inp.B * inp.T,
+            "requests": len(inp.seqlens), "heads": inp.H, "chunk": wl.bt, "in_dtype": wl.in_dtype,
+            "out_dtype": wl.out_dtype, "path": path, "l2": l2}
 
 
 # ---------------------------------------------------------------- our arm
@@ -252,7 +308,7 @@ def run_ours(args, world, rank, local):
     import linear_attention_chunked_02_gb300 as kda
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = ki.WORKLOADS[args.workload]
+    wl = ki.WORKLOADS[args.workload].with_(bt=args.bt)
     inp = ki.build(wl)
     in_dtype, out_dtype = ki.torch_dtype(wl.in_dtype), ki.torch_dtype(wl.out_dtype)
     ine, oute = ELT[wl.in_dtype], ELT[wl.out_dtype]
@@ -260,13 +316,35 @@ def run_ours(args, world, rank, local):
     cu = inp.cu_seqlens.to(dev) if inp.cu_seqlens is not None else None
     nseq = 0 if cu is None else cu.numel() - 1
     out = torch.empty(A.shape, dtype=out_dtype, device=dev)
-    need = kda.workspace_size(inp.B, inp.T, inp.H, nseq)
-    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    need = kda.workspace_size(inp.B, inp.T, inp.H, nseq) if wl.bt == 64 else 0
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev) if wl.bt == 64 else None
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flushes_l2(inp) else None
 
     def step():
         return kda.solve_tril(A, cu, out_dtype=out_dtype, path=args.path, out=out, workspace=ws,
                               stream=stream, return_path=True)
+
+    def timed_steps(n, run):
+        """Device ms of n calls of run(): one event pair around all of them, or,
+        with an L2 flush between calls, one pair per call (flush outside)."""
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                run()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(n)]
+        for e0, e1 in pairs:
+            flush.zero_()
+            e0.record(stream)
+            run()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(e0.elapsed_time(e1) for e0, e1 in pairs)
 
     _, taken = step()
     launches_per_step = 2 if taken == "split" else 1
@@ -281,44 +359,47 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    total_ms = timed_steps(args.steps, step)
     t1 = time.time()
     barrier(world)
-    ms, value = whole_job_gbs(ev0.elapsed_time(ev1) / args.steps, alg, world, dev)
+    ms, value = whole_job_gbs(total_ms / args.steps, alg, world, dev)
     if rank == 0:
         sampler.stop()
         clocks = sampler.summary(t0, t1)
 
-    # end to end: pinned host buffers, copies inside the timed region (C-ABI host entry)
+    # end to end: pinned host buffers, copies inside the timed region (the C-ABI host
+    # entry for 64-token chunks; copies on the stream around solve_tril otherwise)
     A_host = inp.A.pin_memory()
     cu_host = inp.cu_seqlens.pin_memory() if inp.cu_seqlens is not None else None
     Ai_host = torch.empty(A.shape, dtype=out_dtype).pin_memory()
     cu_dev = torch.empty_like(cu) if cu is not None else None
     A_dev = torch.empty_like(A)
+
+    def e2e_step():
+        if wl.bt == 64:
+            kda.solve_tril_host(A_host, Ai_host, A_dev, out, cu_host, cu_dev, ws, stream)
+            return
+        with torch.cuda.stream(stream):
+            A_dev.copy_(A_host, non_blocking=True)
+            if cu_dev is not None:
+                cu_dev.copy_(cu_host, non_blocking=True)
+            kda.solve_tril(A_dev, cu_dev, out_dtype=out_dtype, out=out, stream=stream)
+            Ai_host.copy_(out, non_blocking=True)
+
     e2e_steps = max(3, min(args.steps, 200))
     for _ in range(2):
-        kda.solve_tril_host(A_host, Ai_host, A_dev, out, cu_host, cu_dev, ws, stream)
+        e2e_step()
     torch.cuda.synchronize(dev)
     barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        kda.solve_tril_host(A_host, Ai_host, A_dev, out, cu_host, cu_dev, ws, stream)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    e2e_total = timed_steps(e2e_steps, e2e_step)
     barrier(world)
-    e2e_ms, e2e_value = whole_job_gbs(e0.elapsed_time(e1) / e2e_steps, alg, world, dev)
+    e2e_ms, e2e_value = whole_job_gbs(e2e_total / e2e_steps, alg, world, dev)
 
     if rank != 0:
         return
     peak, peak_kind = hbm_peak()
-    kernel = "kda_tril_kernel<MODE_FUSED>" if taken == "single" else "kda_tril_kernel<MODE_MERGE>"
+    kernel = KERNEL[wl.bt] if taken == "single" else "kda_tril_kernel<MODE_MERGE>"
     achieved = alg / (ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -329,7 +410,7 @@ def run_ours(args, world, rank, local):
         "chunk_heads_per_s": len(inp.chunks()) * inp.H / (ms / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": ncu_traffic(kernel, wl.name), "kernel": kernel,
+                     "traffic": ncu_traffic(kernel, workload_key(wl)), "kernel": kernel,
                      "algorithmic_bytes_per_launch": alg},
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": inp.A.numel() * ine + (0 if cu is None else cu.numel() * 4),
@@ -352,9 +433,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(ki.WORKLOADS))
     ap.add_argument("--path", default="auto", choices=["auto", "single", "split"])
+    ap.add_argument("--bt", type=int, default=64, choices=[16, 32, 64],
+                    help="chunk length (16 and 32: the solver's shorter branches)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="store the DRAM traffic of the launch captured in this ncu --csv log "
+                         "for --workload/--bt in profiles/traffic.json, then exit")
+    ap.add_argument("--ncu-command", default="", help="the command the capture ran (recorded)")
     args = ap.parse_args()
+    if args.record_traffic:
+        wl = ki.WORKLOADS[args.workload].with_(bt=args.bt)
+        print(json.dumps(record_traffic(args.record_traffic, workload_key(wl), KERNEL[args.bt],
+                                        args.ncu_command)))
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
