@@ -11,10 +11,10 @@
 //     TF32, computed transposed as in the 64-token kernel's level A.
 // Persistent CTAs of 64 threads walk chunk-heads q = slot, slot + slots, ...
 // with one slot per unit (16 tokens) or per warp (32 tokens).  Tiles are small
-// (0.5-3 KiB), so each slot streams its own tiles through a STAGES-deep ring in
+// (0.5-3 KiB), so each slot streams its own tiles through a SMALL_STAGES-deep ring in
 // shared memory with cp.async: 16-byte copies, zero-fill for rows past a
 // partial chunk's end (never read), nothing for chunk-heads past the last one.
-// The next STAGES - 1 chunk-heads are in flight while one is computed.  The
+// The next SMALL_STAGES - 1 chunk-heads are in flight while one is computed.  The
 // ring holds the input bytes as they are; with 16-bit input the diagonal
 // blocks are widened once into an FP32 tile (every lane converts its share)
 // and the off-diagonal block is widened in registers by the MMA operand load.
@@ -36,7 +36,9 @@ struct SmallParams {
     int32_t n_tasks;           // loop bound on chunk-head indices
 };
 
-constexpr int SMALL_STAGES = 3;
+// cp.async ring depth per slot: one chunk-head in flight while one is computed
+// (GB300: 2 and 3 stages time the same within 2 %; 2 leaves more registers)
+constexpr int SMALL_STAGES = 2;
 
 // Chunk-heads q = q0, q0 + step, ... of one slot; chunk c = q / H and head
 // h = q % H are advanced incrementally (one division at the start).
@@ -113,7 +115,7 @@ __device__ __forceinline__ void issue16(const SmallParams &p, const Meta &m, TIn
 
 // 16-token chunks: unit u of CTA b solves chunk-heads 4b + u, 4b + u + 4 grid, ...
 template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(NTHREADS, sizeof(TIn) == 2 ? 14 : 16)
+__global__ void __launch_bounds__(NTHREADS, 14)
 kda_bt16_kernel(const SmallParams p) {
     constexpr int S = SMALL_STAGES;
     constexpr bool WIDEN = sizeof(TIn) == 2;
