@@ -139,6 +139,26 @@ def _softplus(x: np.ndarray) -> np.ndarray:
     return np.logaddexp(0.0, x)
 
 
+def _draw_kgb(rng: np.random.Generator, L: int, H: int, kind: str, bt: int = BT, K: int = KEY_DIM):
+    """fp64 (k [L, H, K], beta [L, H], g [L, H, K]) of one slab of L tokens, drawn in
+    the order k, beta pre-activations, g pre-activations; g restarts at every chunk
+    of bt tokens (zero for the "nodecay" kind)."""
+    C = (L + bt - 1) // bt
+    Lp = C * bt
+    k = rng.standard_normal((L, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((L, H))))
+    gpre = rng.standard_normal((L, H, K))
+    if kind == "nodecay":
+        g = np.zeros_like(k)
+    elif kind == "kda":
+        pad = ((0, Lp - L), (0, 0), (0, 0))
+        g = np.cumsum(-_softplus(np.pad(gpre, pad)).reshape(C, bt, H, K), axis=1).reshape(Lp, H, K)[:L]
+    else:
+        raise ValueError(f"unknown input kind {kind!r}")
+    return k, beta, g
+
+
 def _slab(rng: np.random.Generator, L: int, H: int, kind: str, bt: int = BT) -> np.ndarray:
     """fp64 A for one slab of L tokens: [L, H, bt], strictly lower within each chunk of bt."""
     C = (L + bt - 1) // bt
@@ -151,19 +171,11 @@ def _slab(rng: np.random.Generator, L: int, H: int, kind: str, bt: int = BT) -> 
         S = vals.reshape(C, bt, H, bt)                       # [C, i, H, j]
         keep = (col < row)[None, :, None, :]
     else:
-        k = rng.standard_normal((L, H, KEY_DIM))
-        k /= np.linalg.norm(k, axis=-1, keepdims=True)
-        beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((L, H))))
-        gpre = rng.standard_normal((L, H, KEY_DIM))
+        k, beta, g = _draw_kgb(rng, L, H, kind, bt)
         pad = ((0, Lp - L), (0, 0), (0, 0))
         k = np.pad(k, pad).reshape(C, bt, H, KEY_DIM)
+        g = np.pad(g, pad).reshape(C, bt, H, KEY_DIM)
         beta = np.pad(beta, ((0, Lp - L), (0, 0))).reshape(C, bt, H)
-        if kind == "nodecay":
-            g = np.zeros_like(k)
-        elif kind == "kda":
-            g = np.cumsum(-_softplus(np.pad(gpre, pad)).reshape(C, bt, H, KEY_DIM), axis=1)
-        else:
-            raise ValueError(f"unknown input kind {kind!r}")
         # sum_d (k_i e^{g_i})_d (k_j e^{-g_j})_d, batched over chunks and heads.
         q = torch.from_numpy(np.ascontiguousarray((k * np.exp(g)).transpose(0, 2, 1, 3)))
         kk = torch.from_numpy(np.ascontiguousarray((k * np.exp(-g)).transpose(0, 2, 3, 1)))
@@ -213,6 +225,77 @@ def build(wl: Workload, poison: bool = False) -> SolverInput:
     if poison:
         poison_ignored(out)
     return out
+
+
+@dataclass
+class KgbInput:
+    """The inputs the chunk matrices are built from: keys ``k`` [B, T, H, K] and
+    ``beta`` [B, T, H] in the input dtype, and the per-channel cumulative log
+    decay ``g`` [B, T, H, K] in float32 (restarting at every chunk)."""
+
+    workload: Workload
+    k: torch.Tensor
+    g: torch.Tensor
+    beta: torch.Tensor
+    cu_seqlens: Optional[torch.Tensor]
+    seqlens: list = field(default_factory=list)
+
+    @property
+    def B(self) -> int:
+        return self.k.shape[0]
+
+    @property
+    def T(self) -> int:
+        return self.k.shape[1]
+
+    @property
+    def H(self) -> int:
+        return self.k.shape[2]
+
+    @property
+    def K(self) -> int:
+        return self.k.shape[3]
+
+    @property
+    def bt(self) -> int:
+        return BT
+
+    def chunks(self):
+        """(row0, n_valid) of every 64-token chunk, in order (flattened B*T rows)."""
+        return SolverInput.chunks(self)
+
+
+def build_kgb(wl: Workload, K: int = KEY_DIM) -> KgbInput:
+    """Seeded (k, g, beta) for ``wl`` (kinds "kda" and "nodecay"), drawn exactly as
+    for ``build``: with K = 128 and the same workload, the chunk matrices built from
+    them by the KDA construction are the ``A`` that ``build`` returns (before rounding)."""
+    if wl.kind == "gauss":
+        raise ValueError("the gauss kind has no keys and decays")
+    rng = np.random.default_rng(wl.seed)
+    if wl.layout == "dense":
+        lens = [wl.T] * wl.B
+    elif wl.layout == "packed":
+        if wl.ragged is not None:
+            n, lo, hi = wl.ragged
+            lens = [int(x) for x in rng.integers(lo, hi + 1, size=n)]
+        else:
+            lens = [int(x) for x in wl.seqlens]
+    else:
+        raise ValueError(wl.layout)
+    draws = [_draw_kgb(rng, L, wl.H, wl.kind, BT, K) if L > 0 else
+             (np.zeros((0, wl.H, K)), np.zeros((0, wl.H)), np.zeros((0, wl.H, K))) for L in lens]
+    if wl.layout == "dense":
+        k = np.stack([d[0] for d in draws], 0) if lens else np.zeros((0, wl.T, wl.H, K))
+        beta = np.stack([d[1] for d in draws], 0) if lens else np.zeros((0, wl.T, wl.H))
+        g = np.stack([d[2] for d in draws], 0) if lens else np.zeros((0, wl.T, wl.H, K))
+        cu = None
+    else:
+        k = np.concatenate([d[0] for d in draws], 0)[None]
+        beta = np.concatenate([d[1] for d in draws], 0)[None]
+        g = np.concatenate([d[2] for d in draws], 0)[None]
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+    return KgbInput(wl, _round(k, wl.in_dtype).contiguous(), torch.from_numpy(g.astype(np.float32)).contiguous(),
+                    _round(beta, wl.in_dtype).contiguous(), cu, lens)
 
 
 def poison_ignored(inp: SolverInput) -> None:

@@ -32,9 +32,10 @@ def compile_oracle(out_path: str = LIB, plant: int = 0, openmp: bool = True) -> 
     """
     cc = os.environ.get("CC", shutil.which("gcc") or "cc")
     base = [cc, "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
-            f"-DKDA_ORACLE_PLANT={int(plant)}", SRC, "-o", out_path]
+            f"-DKDA_ORACLE_PLANT={int(plant)}", SRC, "-lm", "-o", out_path]
     tmp = out_path + ".tmp"
     cmds = ([base[:-1] + [tmp, "-fopenmp"]] if openmp else []) + [base[:-1] + [tmp]]
+    assert base[-2] == "-o"
     err = ""
     for cmd in cmds:
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -63,6 +64,9 @@ class Oracle:
         lib.kda_oracle_solve_tril_bt.argtypes = [dp, dp, ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                                  ctypes.c_int32, ctypes.c_int32]
         lib.kda_oracle_solve_tril_bt.restype = ctypes.c_int
+        lib.kda_oracle_solve_kgb.argtypes = [dp, dp, dp, dp, dp, ip, ctypes.c_int32, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+        lib.kda_oracle_solve_kgb.restype = ctypes.c_int
         lib.kda_oracle_num_chunks.argtypes = [ip, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]
         lib.kda_oracle_num_chunks.restype = ctypes.c_int64
         lib.kda_oracle_num_threads.restype = ctypes.c_int
@@ -104,6 +108,31 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return Ai
+
+    def solve_kgb(self, k: np.ndarray, g: np.ndarray, beta: np.ndarray,
+                  cu_seqlens: Optional[np.ndarray] = None, return_A: bool = False):
+        """Build every 64-token chunk's A from keys k [B, T, H, K], cumulative log
+        decays g [B, T, H, K] and betas [B, T, H] (any float dtype, upcast exactly)
+        and solve it.  Returns fp64 Ai [B, T, H, 64] (and A if return_A); rows that
+        belong to no chunk are zero."""
+        k64 = np.ascontiguousarray(k, dtype=np.float64)
+        g64 = np.ascontiguousarray(g, dtype=np.float64)
+        b64 = np.ascontiguousarray(beta, dtype=np.float64)
+        assert k64.ndim == 4 and g64.shape == k64.shape and b64.shape == k64.shape[:3]
+        B, T, H, K = k64.shape
+        Ai = np.zeros((B, T, H, BT))
+        A = np.zeros((B, T, H, BT)) if return_A else None
+        if cu_seqlens is not None:
+            cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+            cup = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+            nseq = cu.shape[0] - 1
+        else:
+            cup, nseq = None, 0
+        rc = self.lib.kda_oracle_solve_kgb(self._dptr(k64), self._dptr(g64), self._dptr(b64), self._dptr(Ai),
+                                           self._dptr(A) if A is not None else None, cup, nseq, B, T, H, K)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return (Ai, A) if return_A else Ai
 
     def num_threads(self) -> int:
         return int(self.lib.kda_oracle_num_threads())

@@ -30,9 +30,21 @@
  * used): the definition above is unchanged with 64 replaced by the chunk
  * length bt.
  *
+ * The chunk matrix itself (the _kgb entry point): KDA prefill builds A from the
+ * keys k, the per-token betas and the per-channel cumulative log decays g of
+ * the chunk's tokens, and the same page says KDA prefill opts into the shared
+ * solver.  The construction, written out as its definition with one exp per
+ * term (no factorisation of the decay), is
+ *
+ *     A[i][j] = beta[i] * sum_d k[i][d] * k[j][d] * exp(g[i][d] - g[j][d])
+ *
+ * for j < i < n and zero elsewhere; only differences of g inside one chunk
+ * enter, so g may restart at chunk starts or run on.
+ *
  * Build: plain C99, -O2 -ffp-contract=off (no fused multiply-add, so the x86
  * and Arm builds give identical bits), optional -fopenmp.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -143,6 +155,72 @@ int kda_oracle_solve_tril_bt(const double *A, double *Ai, const int32_t *cu_seql
             for (int i = 0; i < c.n; ++i)
                 memcpy(Ai + (c.row0 + i) * ld + h * bt, X + i * bt, sizeof(double) * bt);
         }
+        free(X);
+    }
+    free(ch);
+    return 0;
+}
+
+/* Chunk matrix of one chunk-head (64 x 64 row-major into M) from the chunk's
+ * rows of k and g (K channels, row stride ldk elements) and beta (row stride
+ * ldb); rows i, j < n are used, everything else of M is zero. */
+static void kda_oracle_kgb_chunk(const double *k, const double *g, const double *beta, int64_t ldk,
+                                 int64_t ldb, int n, int K, double *M)
+{
+    memset(M, 0, sizeof(double) * KDA_ORACLE_BT * KDA_ORACLE_BT);
+    for (int i = 1; i < n; ++i) {
+        for (int j = 0; j < i; ++j) {
+            double s = 0.0;
+            for (int d = 0; d < K; ++d) {
+#if KDA_ORACLE_PLANT == 4
+                const double e = exp(g[j * ldk + d] - g[i * ldk + d]);   /* planted: decay reversed */
+#else
+                const double e = exp(g[i * ldk + d] - g[j * ldk + d]);
+#endif
+                s += k[i * ldk + d] * k[j * ldk + d] * e;
+            }
+#if KDA_ORACLE_PLANT == 5
+            M[i * KDA_ORACLE_BT + j] = beta[j * ldb] * s;                 /* planted: beta of the column */
+#else
+            M[i * KDA_ORACLE_BT + j] = beta[i * ldb] * s;
+#endif
+        }
+    }
+}
+
+/* Build every 64-token chunk's A from k, g, beta and solve it.  k, g: fp64
+ * [rows, H, K]; beta: fp64 [rows, H]; Ai (and A_out if not NULL): fp64
+ * [rows, H, 64], rows = B*T, written on the rows of every chunk only.  Layouts
+ * as for kda_oracle_solve_tril.  Returns 0, or -1 on a bad argument. */
+int kda_oracle_solve_kgb(const double *k, const double *g, const double *beta, double *Ai, double *A_out,
+                         const int32_t *cu_seqlens, int32_t nseq, int64_t B, int64_t T, int32_t H, int32_t K)
+{
+    if (H <= 0 || T < 0 || B < 0 || K < 1) return -1;
+    if (cu_seqlens != NULL && (B != 1 || nseq < 0)) return -1;
+    const int bt = KDA_ORACLE_BT;
+    int64_t nc = kda_oracle_chunks(cu_seqlens, nseq, B, T, bt, NULL, 0);
+    kda_oracle_chunk_t *ch = (kda_oracle_chunk_t *)malloc(sizeof(*ch) * (size_t)(nc > 0 ? nc : 1));
+    if (!ch) return -1;
+    kda_oracle_chunks(cu_seqlens, nseq, B, T, bt, ch, nc);
+    const int64_t ldk = (int64_t)H * K, ldo = (int64_t)H * bt;
+    const int64_t ntask = nc * H;
+#pragma omp parallel
+    {
+        double *M = (double *)malloc(sizeof(double) * bt * bt);
+        double *X = (double *)malloc(sizeof(double) * bt * bt);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t q = 0; q < ntask; ++q) {
+            const kda_oracle_chunk_t c = ch[q / H];
+            const int64_t h = q % H;
+            kda_oracle_kgb_chunk(k + c.row0 * ldk + h * K, g + c.row0 * ldk + h * K, beta + c.row0 * H + h,
+                                 ldk, H, c.n, K, M);
+            kda_oracle_invert_chunk_bt(M, bt, c.n, bt, X);
+            for (int i = 0; i < c.n; ++i) {
+                memcpy(Ai + (c.row0 + i) * ldo + h * bt, X + i * bt, sizeof(double) * bt);
+                if (A_out) memcpy(A_out + (c.row0 + i) * ldo + h * bt, M + i * bt, sizeof(double) * bt);
+            }
+        }
+        free(M);
         free(X);
     }
     free(ch);

@@ -242,8 +242,108 @@ def torch_isnan_any(t) -> bool:
     return bool(torch.isnan(t.float()).any())
 
 
+# ------------------------------- chunk matrices from keys, betas and decays
+KGB_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "kgb_cases.txt")
+
+
+def _load_kgb_golden():
+    lines = [l.strip() for l in open(KGB_GOLDEN) if l.strip() and not l.startswith("#")]
+    cases, i = [], 0
+    while i < len(lines):
+        name = lines[i].split()[1]
+        _, n, _, K = lines[i + 1].split()
+        n, K = int(n), int(K)
+        i += 2
+        blocks = {}
+        for key, rows in (("k", n), ("g", n), ("beta", 1), ("X", n)):
+            assert lines[i] == key, (name, lines[i])
+            blocks[key] = np.array([[float(x) for x in lines[i + 1 + r].split()] for r in range(rows)])
+            i += 1 + rows
+        assert lines[i] == "end"
+        i += 1
+        cases.append((name, n, K, blocks))
+    return cases
+
+
+def _kgb_one(orc, k, g, beta, cu=None):
+    """k, g: [T, K]; beta: [T] for one head of one batch row."""
+    k = np.asarray(k, dtype=np.float64)[None, :, None, :]
+    g = np.asarray(g, dtype=np.float64)[None, :, None, :]
+    beta = np.asarray(beta, dtype=np.float64).reshape(1, -1, 1)
+    Ai, A = orc.solve_kgb(k, g, beta, cu, return_A=True)
+    return Ai[0, :, 0, :], A[0, :, 0, :]
+
+
+def check_kgb_golden(orc):
+    """Hand-worked (k, g, beta) -> X cases (tests/golden/kgb_cases.txt)."""
+    for name, n, K, b in _load_kgb_golden():
+        Ai, _ = _kgb_one(orc, b["k"], b["g"], b["beta"][0])
+        assert np.abs(Ai[:n, :n] - b["X"]).max() <= 1e-15, name
+        assert np.all(Ai[:n, n:] == 0), name
+
+
+def check_kgb_nodecay(orc):
+    """g = 0: A is beta_i (K K^T)_ij below the diagonal (a plain matrix product)."""
+    rng = np.random.default_rng(7)
+    for T, K in ((64, 128), (50, 32), (130, 8)):
+        k = rng.standard_normal((T, K))
+        beta = rng.uniform(0.1, 1.0, T)
+        _, A = _kgb_one(orc, k, np.zeros((T, K)), beta)
+        for t0 in range(0, T, BT):
+            n = min(BT, T - t0)
+            kc = k[t0:t0 + n]
+            want = np.tril(beta[t0:t0 + n, None] * (kc @ kc.T), -1)
+            assert np.abs(A[t0:t0 + n, :n] - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+            assert np.all(A[t0:t0 + n, n:] == 0)
+
+
+def check_kgb_decay_closed_form(orc):
+    """One-hot keys, beta = 1, g_t = -lam * t on every channel: A[i][j] = r^(i-j)
+    with r = exp(-lam), so I + A = (I - r S)^-1 and the inverse is I - r S
+    (S = ones on the subdiagonal), in every chunk, full or partial."""
+    for lam, T, K in ((0.3, 64, 4), (1.0, 100, 1), (0.05, 37, 16)):
+        k = np.zeros((T, K))
+        k[:, 0] = 1.0
+        g = -lam * np.arange(T, dtype=np.float64)[:, None] * np.ones((1, K))
+        Ai, _ = _kgb_one(orc, k, g, np.ones(T))
+        r = np.exp(-lam)
+        for t0 in range(0, T, BT):
+            n = min(BT, T - t0)
+            want = np.eye(n) - r * np.eye(n, k=-1)
+            assert np.abs(Ai[t0:t0 + n, :n] - want).max() <= 1e-13, (lam, t0)
+
+
+def check_kgb_shift_invariance(orc):
+    """Only differences of g inside a chunk enter: g + c (c per channel) changes nothing."""
+    wl = ki.Workload("pin", "dense", H=2, in_dtype="f32", out_dtype="f32", seed=43, B=1, T=90)
+    x = ki.build_kgb(wl, K=16)
+    k, g, beta = (orc_mod.to_f64(t) for t in (x.k, x.g, x.beta))
+    c = np.random.default_rng(3).uniform(-5, 5, (1, 1, 2, 16))
+    a = orc.solve_kgb(k, g, beta)
+    b = orc.solve_kgb(k, g + c, beta)
+    assert np.abs(a - b).max() <= 1e-12
+
+
+def check_kgb_generator(orc):
+    """The oracle's per-term definition against the generator's factorised matrix
+    product (exp(g_i) and exp(-g_j) split) on the same fp64 draws, and the solve
+    against the plain solver oracle on that matrix."""
+    for kind in ("kda", "nodecay"):
+        rng = np.random.default_rng(11)
+        L, H = 150, 2
+        k, beta, g = ki._draw_kgb(rng, L, H, kind)
+        A_gen = ki._slab(np.random.default_rng(11), L, H, kind)
+        Ai, A = orc.solve_kgb(k[None], g[None], beta[None], return_A=True)
+        assert np.abs(A[0] - A_gen).max() <= 1e-12, kind
+        Ai2 = orc.solve_tril(A_gen[None])
+        assert np.abs(Ai - Ai2).max() <= 1e-11, kind
+
+
+KGB_CHECKS = [check_kgb_golden, check_kgb_nodecay, check_kgb_decay_closed_form,
+              check_kgb_shift_invariance, check_kgb_generator]
+
 ALL_CHECKS = [check_golden, check_worked_small, check_rational, check_closed_form,
-              check_exact_64, check_residual, check_layout, check_poison]
+              check_exact_64, check_residual, check_layout, check_poison] + KGB_CHECKS
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -261,6 +361,10 @@ PLANTS = {
     2: ("wrong sign of the off-diagonal entries", ["check_golden", "check_worked_small",
                                                     "check_rational", "check_closed_form"]),
     3: ("packed chunk boundary shifted by one token", ["check_layout"]),
+    4: ("decay exponent reversed", ["check_kgb_golden", "check_kgb_decay_closed_form",
+                                    "check_kgb_generator"]),
+    5: ("beta of the column instead of the row", ["check_kgb_golden", "check_kgb_nodecay",
+                                                   "check_kgb_generator"]),
 }
 
 
