@@ -139,7 +139,8 @@ def hbm_peak():
 # sources that define each kernel family and its launch
 _COMMON_SOURCES = ["kda_kernels.cuh", "kda_launch.cuh", "kda_api.cu", "kda_inst_f32.cu",
                    "kda_inst_bf16.cu", "kda_inst_f16.cu"]
-KERNEL_SOURCES = {"kda_tril_kernel": _COMMON_SOURCES, "kda_bt": _COMMON_SOURCES + ["kda_small.cuh"]}
+KERNEL_SOURCES = {"kda_tril_kernel": _COMMON_SOURCES, "kda_bt": _COMMON_SOURCES + ["kda_small.cuh"],
+                  "kda_kgb": _COMMON_SOURCES + ["kda_small.cuh", "kda_kgb.cuh"]}
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -304,6 +305,179 @@ def config_dict(inp: ki.SolverInput, path: str):
 
 
 # ---------------------------------------------------------------- our arm
+def timed_calls(n, run, stream, dev, flush):
+    """Device ms of n calls of run(): one event pair around all of them, or, with
+    an L2 flush buffer, one pair per call with the flush outside it."""
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for e0, e1 in pairs:
+        flush.zero_()
+        e0.record(stream)
+        run()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(e0.elapsed_time(e1) for e0, e1 in pairs)
+
+
+# ------------------------------------------- fused construction + solve (kgb)
+KGB_KERNEL = "kda_kgb_kernel"
+
+
+def kgb_bytes(x: ki.KgbInput, in_elt: int, out_elt: int) -> int:
+    """Minimum HBM bytes of one fused solve: every row's keys, decays and beta, and
+    the chunks' output rows."""
+    rows = x.B * x.T
+    return rows * x.H * (x.K * in_elt + x.K * 4 + in_elt) + sum(n for _, n in x.chunks()) * x.H * 64 * out_elt
+
+
+def kgb_config(x: ki.KgbInput):
+    wl = x.workload
+    mb = kgb_bytes(x, ELT[wl.in_dtype], ELT[wl.out_dtype]) / 1e6
+    return {"workload": f"{wl.name}_kgb", "layout": wl.layout, "tokens": x.B * x.T, "requests": len(x.seqlens),
+            "heads": x.H, "key_dim": x.K, "chunk": 64, "in_dtype": wl.in_dtype, "out_dtype": wl.out_dtype,
+            "op": "chunk matrix from k, g, beta fused with the solve",
+            "l2": f"inputs+output {mb:.0f} MB > 129 MB L2; no flush between steps"}
+
+
+def time_oracle_kgb(x: ki.KgbInput, seconds: float, alg_bytes: int):
+    import oracle
+    orc = oracle.get()
+    k, g, b = (oracle.to_f64(t) for t in (x.k, x.g, x.beta))
+    cu = x.cu_seqlens.numpy() if x.cu_seqlens is not None else None
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        orc.solve_kgb(k, g, b, cu)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return alg_bytes * reps / el / 1e9, reps, el, orc.num_threads()
+
+
+def run_ours_kgb(args, world, rank, local):
+    import linear_attention_chunked_02_gb300 as kda
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = ki.WORKLOADS[args.workload]
+    x = ki.build_kgb(wl)
+    out_dtype = ki.torch_dtype(wl.out_dtype)
+    ine, oute = ELT[wl.in_dtype], ELT[wl.out_dtype]
+    k, g, b = x.k.to(dev), x.g.to(dev), x.beta.to(dev)
+    cu = x.cu_seqlens.to(dev) if x.cu_seqlens is not None else None
+    out = torch.empty((x.B, x.T, x.H, 64), dtype=out_dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.solve_tril_kgb(k, g, b, cu, out_dtype=out_dtype, out=out, stream=stream)
+
+    alg = kgb_bytes(x, ine, oute)
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = time.time()
+    total = timed_calls(args.steps, step, stream, dev, None)
+    t1 = time.time()
+    barrier(world)
+    ms, value = whole_job_gbs(total / args.steps, alg, world, dev)
+    if rank == 0:
+        sampler.stop()
+        clocks = sampler.summary(t0, t1)
+
+    # end to end: pinned host inputs copied in and the output copied back every step
+    hk, hg, hb = x.k.pin_memory(), x.g.pin_memory(), x.beta.pin_memory()
+    hcu = x.cu_seqlens.pin_memory() if x.cu_seqlens is not None else None
+    hout = torch.empty(out.shape, dtype=out_dtype).pin_memory()
+    dk, dg, db = torch.empty_like(k), torch.empty_like(g), torch.empty_like(b)
+    dcu = torch.empty_like(cu) if cu is not None else None
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dk.copy_(hk, non_blocking=True)
+            dg.copy_(hg, non_blocking=True)
+            db.copy_(hb, non_blocking=True)
+            if dcu is not None:
+                dcu.copy_(hcu, non_blocking=True)
+            kda.solve_tril_kgb(dk, dg, db, dcu, out_dtype=out_dtype, out=out, stream=stream)
+            hout.copy_(out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 100))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms, e2e_value = whole_job_gbs(timed_calls(e2e_steps, e2e_step, stream, dev, None) / e2e_steps, alg,
+                                      world, dev)
+    if rank != 0:
+        return
+    peak, peak_kind = hbm_peak()
+    achieved = alg / (ms / 1e3) / 1e9
+    key = f"{wl.name}_kgb"
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.in_dtype, "data": "synthetic", "config": kgb_config(x),
+        "chunk_heads_per_s": len(x.chunks()) * x.H / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": ncu_traffic(KGB_KERNEL, key), "kernel": KGB_KERNEL,
+                     "algorithmic_bytes_per_launch": alg},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x.k.numel() * ine + x.g.numel() * 4 + x.beta.numel() * ine
+                + (0 if cu is None else cu.numel() * 4),
+                "d2h_bytes_per_step": out.numel() * oute},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, reps, el, cores = time_oracle_kgb(x, args.cpu_seconds, alg)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{reps} solves of the full workload in {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_kgb(args, world, rank):
+    """The oracle of the fused path, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    wl = ki.WORKLOADS[args.workload]
+    x = ki.build_kgb(wl)
+    alg = kgb_bytes(x, ELT[wl.in_dtype], ELT[wl.out_dtype])
+    import oracle
+    orc = oracle.get()
+    k, g, b = (oracle.to_f64(t) for t in (x.k, x.g, x.beta))
+    cu = x.cu_seqlens.numpy() if x.cu_seqlens is not None else None
+    for _ in range(args.warmup):
+        orc.solve_kgb(k, g, b, cu)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.solve_kgb(k, g, b, cu)
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    v = alg / (ms / 1e3) / 1e9
+    sample = f"the full workload ({len(x.chunks()) * x.H} chunk-heads) per step, fp64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": kgb_config(x),
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, world, rank, local):
     import linear_attention_chunked_02_gb300 as kda
     torch.cuda.set_device(local)
@@ -326,25 +500,7 @@ def run_ours(args, world, rank, local):
                               stream=stream, return_path=True)
 
     def timed_steps(n, run):
-        """Device ms of n calls of run(): one event pair around all of them, or,
-        with an L2 flush between calls, one pair per call (flush outside)."""
-        if flush is None:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(n):
-                run()
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            return e0.elapsed_time(e1)
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(n)]
-        for e0, e1 in pairs:
-            flush.zero_()
-            e0.record(stream)
-            run()
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        return sum(e0.elapsed_time(e1) for e0, e1 in pairs)
+        return timed_calls(n, run, stream, dev, flush)
 
     _, taken = step()
     launches_per_step = 2 if taken == "split" else 1
@@ -435,6 +591,9 @@ def main():
     ap.add_argument("--path", default="auto", choices=["auto", "single", "split"])
     ap.add_argument("--bt", type=int, default=64, choices=[16, 32, 64],
                     help="chunk length (16 and 32: the solver's shorter branches)")
+    ap.add_argument("--op", default="solve", choices=["solve", "kgb"],
+                    help="kgb: the chunk matrix built from keys, decays and betas (128 channels) "
+                         "fused with the 64-token solve")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
@@ -444,17 +603,17 @@ def main():
     args = ap.parse_args()
     if args.record_traffic:
         wl = ki.WORKLOADS[args.workload].with_(bt=args.bt)
-        print(json.dumps(record_traffic(args.record_traffic, workload_key(wl), KERNEL[args.bt],
-                                        args.ncu_command)))
+        key, kernel = ((f"{wl.name}_kgb", KGB_KERNEL) if args.op == "kgb" else (workload_key(wl), KERNEL[args.bt]))
+        print(json.dumps(record_traffic(args.record_traffic, key, kernel, args.ncu_command)))
         return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         world, rank, _ = dist_setup(nccl=False)
-        run_reference(args, world, rank)
+        (run_reference_kgb if args.op == "kgb" else run_reference)(args, world, rank)
         return
     world, rank, local = dist_setup(nccl=True)
-    run_ours(args, world, rank, local)
+    (run_ours_kgb if args.op == "kgb" else run_ours)(args, world, rank, local)
 
 
 if __name__ == "__main__":

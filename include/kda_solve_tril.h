@@ -240,6 +240,41 @@ KDA_API kda_status_t kda_solve_tril_bt(const void *A, void *Ai, const int32_t *c
                                        int32_t num_seqs, int64_t B, int64_t T, int32_t H, int32_t bt,
                                        int32_t in_dtype, int32_t out_dtype, void *stream);
 
+/*
+ * The 64-token solve with the chunk matrix built on chip from the quantities
+ * KDA prefill builds it from (the same page says KDA prefill opts into the
+ * shared solver):
+ *
+ *     A[i][j] = beta[i] * sum_d k[i][d] * k[j][d] * exp(g[i][d] - g[j][d])   (j < i),
+ *
+ * per chunk and head, for the chunk's token rows i, j; Ai = (I + A)^-1 is
+ * written as by kda_solve_tril.  A itself is never stored.
+ *
+ *   k           device, [B, T, H, K] of in_dtype (keys), 16-byte aligned.
+ *   g           device, [B, T, H, K] float32: per-channel cumulative log decay;
+ *               only differences inside a chunk are used, so g may restart at
+ *               chunk starts or run on.  16-byte aligned.  Within any 16-token
+ *               block of a chunk, g may fall by at most 80 per channel (larger
+ *               drops overflow FP32 and give non-finite results).
+ *   beta        device, [B, T, H] of in_dtype, aligned to its element size.
+ *   Ai          device, [B, T, H, 64] of out_dtype, 16-byte aligned; must not
+ *               overlap k, g or beta.
+ *   cu_seqlens, num_seqs, B, T, H, stream: as for kda_solve_tril (layouts,
+ *               partial last chunks, size limits).
+ *   K           channels: 32, 64, 96 or 128 (KDA_ERR_UNSUPPORTED otherwise).
+ *   in_dtype    KDA_F32 / KDA_BF16 / KDA_F16 for k and beta (widened to FP32).
+ *   out_dtype   KDA_F32 / KDA_BF16 / KDA_F16.
+ *
+ * Computes in FP32 (exp, split-TF32 tensor-core products with FP32
+ * accumulation, the solve of kda_solve_tril); within 2e-5*(1+|ref|) of the
+ * exact inverse of the matrix built from the given (rounded) inputs on the
+ * specified workloads.
+ */
+KDA_API kda_status_t kda_solve_tril_kgb(const void *k, const float *g, const void *beta, void *Ai,
+                                        const int32_t *cu_seqlens, int32_t num_seqs, int64_t B, int64_t T,
+                                        int32_t H, int32_t K, int32_t in_dtype, int32_t out_dtype,
+                                        void *stream);
+
 /* Static description of a status code (never NULL). */
 KDA_API const char *kda_status_string(int32_t status);
 

@@ -115,6 +115,41 @@ def solve_tril(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
     return out
 
 
+def solve_tril_kgb(k: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                   cu_seqlens: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+                   out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Per 64-token chunk-head, (I + A)^-1 for the chunk matrix built on chip from
+    keys k [B, T, H, K], cumulative log decays g [B, T, H, K] (float32) and betas
+    [B, T, H]: A[i][j] = beta_i sum_d k_id k_jd exp(g_id - g_jd), j < i.  k and beta
+    share a dtype (float32 / bfloat16 / float16); K is 32, 64, 96 or 128."""
+    for name, t in (("k", k), ("g", g), ("beta", beta)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    if k.dim() != 4 or g.shape != k.shape or beta.shape != k.shape[:3]:
+        raise ValueError(f"shapes k {tuple(k.shape)}, g {tuple(g.shape)}, beta {tuple(beta.shape)} do not match")
+    if k.dtype not in DTYPE_CODE or beta.dtype != k.dtype or g.dtype != torch.float32 or out_dtype not in DTYPE_CODE:
+        raise ValueError(f"unsupported dtypes k {k.dtype}, g {g.dtype}, beta {beta.dtype} -> {out_dtype}")
+    k, g, beta = k.contiguous(), g.contiguous(), beta.contiguous()
+    B, T, H, K = k.shape
+    nseq = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        cu_seqlens = cu_seqlens.contiguous()
+    shape = (B, T, H, BT)
+    if out is None:
+        out = torch.empty(shape, dtype=out_dtype, device=k.device)
+    elif tuple(out.shape) != shape or out.dtype != out_dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, T, H, 64] tensor of out_dtype")
+    with torch.cuda.device(k.device):
+        st = lib().kda_solve_tril_kgb(
+            k.data_ptr(), g.data_ptr(), beta.data_ptr(), out.data_ptr(),
+            cu_seqlens.data_ptr() if cu_seqlens is not None else None, nseq, B, T, H, K,
+            DTYPE_CODE[k.dtype], DTYPE_CODE[out_dtype], _stream_ptr(stream, k.device))
+    _check(st, "kda_solve_tril_kgb")
+    return out
+
+
 def solve_tril_host(A_host: torch.Tensor, Ai_host: torch.Tensor, A_dev: torch.Tensor, Ai_dev: torch.Tensor,
                     cu_seqlens_host: Optional[torch.Tensor] = None, cu_dev: Optional[torch.Tensor] = None,
                     workspace: Optional[torch.Tensor] = None,

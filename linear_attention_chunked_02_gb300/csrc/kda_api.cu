@@ -384,6 +384,49 @@ kda_status_t kda_solve_tril_bt(const void *A, void *Ai, const int32_t *cu_seqlen
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_solve_tril_kgb(const void *k, const float *g, const void *beta, void *Ai,
+                                const int32_t *cu_seqlens, int32_t num_seqs, int64_t B, int64_t T, int32_t H,
+                                int32_t K, int32_t in_dtype, int32_t out_dtype, void *stream) {
+    kda_status_t st = check_args(k, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype);
+    if (st != KDA_OK) return st;
+    if (K != 32 && K != 64 && K != 96 && K != 128) return KDA_ERR_UNSUPPORTED;
+    if (B == 0 || T == 0) return KDA_OK;
+    if (g == nullptr || beta == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t rows = size_t(B) * size_t(T);
+    const size_t kb = rows * size_t(H) * size_t(K) * elt_size(in_dtype), gbytes = rows * size_t(H) * size_t(K) * 4;
+    const size_t bb = rows * size_t(H) * elt_size(in_dtype), ob = rows * size_t(H) * kda::BT * elt_size(out_dtype);
+    if (!aligned16(k) || !aligned16(g) || !aligned16(Ai) ||
+        (reinterpret_cast<uintptr_t>(beta) % uintptr_t(elt_size(in_dtype))) != 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (overlaps(Ai, ob, k, kb) || overlaps(Ai, ob, g, gbytes) || overlaps(Ai, ob, beta, bb))
+        return KDA_ERR_INVALID_ARGUMENT;
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+    DeviceInfo info;
+    if (device_info(device, info) != cudaSuccess) return KDA_ERR_CUDA;
+    kda::KgbParams p;
+    p.k = k;
+    p.g = g;
+    p.beta = beta;
+    p.out = Ai;
+    p.cu = cu_seqlens;
+    p.nseq = num_seqs;
+    p.H = H;
+    p.T = T;
+    p.cpr = static_cast<int32_t>((T + kda::BT - 1) / kda::BT);
+    p.n_tasks = static_cast<int32_t>(max_chunks(B, T, num_seqs) * H);
+    p.K = K;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (in_dtype) {
+        case KDA_F32: e = kda::launch_kgb_f32(out_dtype, p, device, info.num_sms, s); break;
+        case KDA_BF16: e = kda::launch_kgb_bf16(out_dtype, p, device, info.num_sms, s); break;
+        default: e = kda::launch_kgb_f16(out_dtype, p, device, info.num_sms, s); break;
+    }
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char *kda_status_string(int32_t status) {
     switch (status) {
         case KDA_OK: return "ok";

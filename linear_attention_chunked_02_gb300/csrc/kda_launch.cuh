@@ -7,6 +7,7 @@
 
 #include "kda_kernels.cuh"
 #include "kda_small.cuh"
+#include "kda_kgb.cuh"
 
 namespace kda {
 
@@ -125,6 +126,49 @@ cudaError_t launch_small_in(int bt, int out_dtype, const SmallParams &p, int dev
     }
 }
 
+// ------------------------------------ chunk matrix from keys, betas, decays
+template <typename TIn, typename TOut>
+struct KgbKernel {
+    static int blocks_per_sm(int device, cudaError_t &err) {
+        static std::mutex mu;
+        static int cached[64] = {0};
+        std::lock_guard<std::mutex> lock(mu);
+        err = cudaSuccess;
+        if (device < 0 || device >= 64) {
+            err = cudaErrorInvalidDevice;
+            return 0;
+        }
+        if (cached[device] > 0) return cached[device];
+        auto fn = kda_kgb_kernel<TIn, TOut>;
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, KGB_BYTES);
+        if (err != cudaSuccess) return 0;
+        int occ = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, KGB_THREADS, KGB_BYTES);
+        if (err != cudaSuccess) return 0;
+        cached[device] = occ > 0 ? occ : 1;
+        return cached[device];
+    }
+    static cudaError_t launch(const KgbParams &p, int device, int num_sms, cudaStream_t stream) {
+        cudaError_t err;
+        const int occ = blocks_per_sm(device, err);
+        if (err != cudaSuccess) return err;
+        long long grid = (long long)num_sms * occ;
+        if (grid > p.n_tasks) grid = p.n_tasks;
+        if (grid < 1) return cudaSuccess;
+        kda_kgb_kernel<TIn, TOut><<<(unsigned)grid, KGB_THREADS, KGB_BYTES, stream>>>(p);
+        return cudaGetLastError();
+    }
+};
+
+template <typename TIn>
+cudaError_t launch_kgb_in(int out_dtype, const KgbParams &p, int device, int num_sms, cudaStream_t stream) {
+    switch (out_dtype) {
+        case 0: return KgbKernel<TIn, float>::launch(p, device, num_sms, stream);
+        case 1: return KgbKernel<TIn, __nv_bfloat16>::launch(p, device, num_sms, stream);
+        default: return KgbKernel<TIn, __half>::launch(p, device, num_sms, stream);
+    }
+}
+
 // defined in kda_inst_{f32,bf16,f16}.cu
 cudaError_t launch_f32(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
 cudaError_t launch_bf16(int mode, int out_dtype, const Maps &, const Params &, int, int, cudaStream_t);
@@ -132,5 +176,8 @@ cudaError_t launch_f16(int mode, int out_dtype, const Maps &, const Params &, in
 cudaError_t launch_small_f32(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
 cudaError_t launch_small_bf16(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
 cudaError_t launch_small_f16(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
+cudaError_t launch_kgb_f32(int out_dtype, const KgbParams &, int, int, cudaStream_t);
+cudaError_t launch_kgb_bf16(int out_dtype, const KgbParams &, int, int, cudaStream_t);
+cudaError_t launch_kgb_f16(int out_dtype, const KgbParams &, int, int, cudaStream_t);
 
 }  // namespace kda

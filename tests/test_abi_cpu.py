@@ -158,3 +158,33 @@ def test_chunk_length_entry_no_gpu(L):
         pytest.skip("a GPU is present")
     for bt in (16, 32, 64):
         assert call_bt(L, bt=bt, A=1 << 20, Ai=1 << 24) == CUDA
+
+
+def call_kgb(L, k=1 << 20, g=1 << 22, beta=1 << 24, Ai=1 << 26, cu=None, nseq=0, B=1, T=64, H=1, K=128,
+             ind=0, outd=0):
+    return L.kda_solve_tril_kgb(k, g, beta, Ai, cu, nseq, B, T, H, K, ind, outd, None)
+
+
+def test_kgb_entry_checks(L):
+    for K in (0, 16, 48, 160, 256):
+        assert call_kgb(L, K=K) == UNSUPPORTED
+    assert call_kgb(L, ind=5) == UNSUPPORTED
+    assert call_kgb(L, outd=5) == UNSUPPORTED
+    assert call_kgb(L, H=0) == INVALID
+    assert call_kgb(L, cu=4096, nseq=1, B=2) == INVALID
+    assert call_kgb(L, g=None) == INVALID
+    assert call_kgb(L, beta=None) == INVALID
+    assert call_kgb(L, k=None) == INVALID
+    assert call_kgb(L, g=(1 << 22) + 4) == INVALID                # misaligned g
+    assert call_kgb(L, beta=(1 << 24) + 2) == INVALID             # fp32 beta not 4-byte aligned
+    assert call_kgb(L, beta=(1 << 24) + 2, ind=1) != INVALID      # bf16 beta: 2-byte alignment is enough
+    assert call_kgb(L, Ai=(1 << 20) + 64 * 128 * 4 - 16) == INVALID   # Ai overlaps k
+    assert call_kgb(L, T=0) == OK and call_kgb(L, B=0) == OK
+    assert call_kgb(L, H=1 << 19) == UNSUPPORTED
+
+
+def test_kgb_entry_no_gpu(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_kgb(L) == CUDA
