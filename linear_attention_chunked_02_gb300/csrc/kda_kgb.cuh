@@ -36,6 +36,9 @@
 
 namespace kda {
 
+// factor rows per slice: the six block pairs I > J, then a row of ones (I == J)
+constexpr int KGB_FROWS = 7;
+
 struct KgbParams {
     const void *k;             // [rows, H, K], input dtype
     const float *g;            // [rows, H, K]
@@ -54,7 +57,7 @@ constexpr int KGB_THREADS = 128;
 constexpr int KGB_SP = 36;                     // slice row pitch (floats): conflict-free fragments
 constexpr int KGB_SLICE = 64 * KGB_SP;         // floats per slice buffer
 constexpr int KGB_FLOATS = 2 * 4 * KGB_SLICE   // Q and P slices
-                         + 4 * 6 * 32          // f_IJ per slice and block pair
+                         + 4 * KGB_FROWS * 32  // f_IJ per slice and block pair, and a row of ones
                          + 10 * 256            // A blocks, pitch 16
                          + 4 * XTS + 4 * XRS   // inverse tiles of the merge
                          + 64;                 // beta of the chunk's rows
@@ -114,16 +117,28 @@ __device__ __forceinline__ void kgb_issue(const KgbParams &p, const Meta &m, int
 
 // Lane d of the slice's warp: the block-pair factors of channel d, then Q and
 // P of channel d in place (column d of the slice is touched by this lane only).
+// 2^x on the SFU (PTX ex2.approx.ftz.f32; relative error about 2^-22)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <typename TIn>
 __device__ __forceinline__ void kgb_transform(float *kb, float *gb, float *fac, int n, int d) {
     // f_IJ = exp(g_rI - g_rJ), I > J (zero when block I starts past the chunk's end)
+    // exponents are differences of g taken first (exact for nearby values), then
+    // scaled to base 2, so their error does not grow with |g|
+    constexpr float LOG2E = 1.4426950408889634f;
     float gr[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) gr[b] = gb[16 * b * KGB_SP + d];
 #pragma unroll
     for (int I = 1; I < 4; ++I)
 #pragma unroll
-        for (int J = 0; J < I; ++J) fac[(I * (I - 1) / 2 + J) * 32 + d] = 16 * I < n ? __expf(gr[I] - gr[J]) : 0.f;
+        for (int J = 0; J < I; ++J)
+            fac[(I * (I - 1) / 2 + J) * 32 + d] = 16 * I < n ? ex2((gr[I] - gr[J]) * LOG2E) : 0.f;
+    fac[6 * 32 + d] = 1.f;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         float kv[16];
@@ -140,10 +155,10 @@ __device__ __forceinline__ void kgb_transform(float *kb, float *gb, float *fac, 
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int r = 16 * b + i;
-            const float gv = gb[r * KGB_SP + d];
             const bool live = r < n;
-            kb[r * KGB_SP + d] = live ? kv[i] * __expf(gv - gr[b]) : 0.f;
-            gb[r * KGB_SP + d] = live ? kv[i] * __expf(gr[b] - gv) : 0.f;
+            const float e = (gb[r * KGB_SP + d] - gr[b]) * LOG2E;
+            kb[r * KGB_SP + d] = live ? kv[i] * ex2(e) : 0.f;
+            gb[r * KGB_SP + d] = live ? kv[i] * ex2(-e) : 0.f;
         }
     }
 }
@@ -153,16 +168,16 @@ __device__ __forceinline__ void kgb_block(const float *kq, const float *gp, cons
                                           float *Ab, int I, int J, int nsl, int n, int g, int t) {
     TileC c;
     zero(c);
-    const int pr = I > J ? I * (I - 1) / 2 + J : -1;
+    const int pr = I > J ? I * (I - 1) / 2 + J : 6;       // 6: the row of ones
     for (int s = 0; s < nsl; ++s) {
         const float *q0 = kq + s * KGB_SLICE + (16 * I + g) * KGB_SP;
         const float *q1 = q0 + 8 * KGB_SP;
         const float *pb = gp + s * KGB_SLICE + (16 * J + g) * KGB_SP;
-        const float *fs = fac + (s * 6 + (pr < 0 ? 0 : pr)) * 32;
+        const float *fs = fac + (s * KGB_FROWS + pr) * 32;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             const int d0 = 8 * ks + t, d1 = d0 + 4;
-            const float f0 = pr < 0 ? 1.f : fs[d0], f1 = pr < 0 ? 1.f : fs[d1];
+            const float f0 = fs[d0], f1 = fs[d1];
             uint32_t ah[4], al[4];
             split_tf32(q0[d0] * f0, ah[0], al[0]);
             split_tf32(q1[d0] * f0, ah[1], al[1]);
@@ -291,7 +306,7 @@ kda_kgb_kernel(const KgbParams p) {
     float *kq = sm;                                    // Q slices
     float *gp = kq + 4 * KGB_SLICE;                    // P slices
     float *fac = gp + 4 * KGB_SLICE;
-    float *Ab = fac + 4 * 6 * 32;
+    float *Ab = fac + 4 * KGB_FROWS * 32;
     float *Xt = Ab + 10 * 256;
     float *Xr = Xt + 4 * XTS;
     float *bs = Xr + 4 * XRS;
@@ -318,7 +333,7 @@ kda_kgb_kernel(const KgbParams p) {
         }
         cp_async_wait<0>();
         __syncwarp();
-        if (has_slice) kgb_transform<TIn>(kb, gb, fac + warp * 6 * 32, cur.n, lane);
+        if (has_slice) kgb_transform<TIn>(kb, gb, fac + warp * KGB_FROWS * 32, cur.n, lane);
         if (warp == 0) {
             bs[lane] = b0;
             bs[lane + 32] = b1;

@@ -112,6 +112,16 @@ def test_kgb_decay_closed_form(kda):
             assert np.all(got[t0:t0 + n, h, n:] == 0)
 
 
+def test_kgb_large_decay_offset(kda, orc):
+    """g may run on across chunks: a large per-channel offset (rounded to fp32 in
+    the input the oracle also sees) changes nothing beyond the tolerance."""
+    x = ki.build_kgb(ki.Workload("off", "packed", H=3, in_dtype="f32", out_dtype="f32", seed=12,
+                                 seqlens=(64, 100, 17)))
+    off = torch.from_numpy(np.random.default_rng(5).uniform(-900, -300, (1, 1, 3, 128)).astype(np.float32))
+    y = ki.KgbInput(x.workload, x.k, (x.g + off).contiguous(), x.beta, x.cu_seqlens, x.seqlens)
+    check(y, run(kda, y), reference(orc, y), F32, "offset")
+
+
 def test_kgb_residual(kda, orc):
     x = ki.build_kgb(ki.Workload("res", "packed", H=4, in_dtype="f32", out_dtype="f32", seed=31,
                                  seqlens=(64, 100, 33)))
