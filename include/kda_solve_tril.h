@@ -74,7 +74,7 @@ typedef enum {
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARGUMENT = 1, /* bad pointer, size, alignment, overlap or layout */
-    KDA_ERR_UNSUPPORTED = 2,      /* dtype or size this build does not handle */
+    KDA_ERR_UNSUPPORTED = 2,      /* dtype or size the library does not handle */
     KDA_ERR_WORKSPACE = 3,        /* split path forced with a missing or too small workspace */
     KDA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
     KDA_ERR_DEVICE = 5            /* kda_device_error() found a recorded device-side error */
@@ -91,7 +91,7 @@ typedef enum {
  * measurements: the single-pass kernel already inverts the four diagonal
  * blocks in parallel inside one CTA, so splitting only adds the workspace round
  * trip and a launch, and it was slower at every size measured (64 to 131072
- * rows); the threshold therefore lies above any size this build supports. */
+ * rows); the threshold therefore lies above any size the library supports. */
 #define KDA_SPLIT_MIN_TOKENS (INT64_C(1) << 32)
 
 /*

@@ -240,7 +240,7 @@ int64_t kda_oracle_num_chunks(const int32_t *cu_seqlens, int32_t nseq, int64_t B
     return kda_oracle_chunks(cu_seqlens, nseq, B, T, KDA_ORACLE_BT, NULL, 0);
 }
 
-/* Threads an OpenMP parallel region of this build uses (1 without OpenMP). */
+/* Threads an OpenMP parallel region of this library uses (1 without OpenMP). */
 int kda_oracle_num_threads(void)
 {
 #ifdef _OPENMP

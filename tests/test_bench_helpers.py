@@ -1,0 +1,85 @@
+"""bench.py's byte models and its ncu traffic recorder, on CPU."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import kda_inputs as ki  # noqa: E402
+
+
+def test_sector_model():
+    # row i of a chunk reads its first i elements, rounded up to 32-byte sectors
+    assert bench.sector_read_bytes(1, 4) == 0
+    assert bench.sector_read_bytes(2, 4) == 32
+    assert bench.sector_read_bytes(64, 4) == sum(-(-(4 * i) // 32) * 32 for i in range(64)) == 8960
+    assert bench.sector_read_bytes(64, 2) == 4992
+
+
+@pytest.mark.parametrize("bt", [16, 32, 64])
+def test_algorithmic_bytes_per_chunk_length(bt):
+    wl = ki.Workload("b", "packed", H=2, in_dtype="f32", out_dtype="bf16", seed=1, seqlens=(bt, 3), bt=bt)
+    inp = ki.build(wl)
+    want = 2 * (bench.sector_read_bytes(bt, 4) + bt * bt * 2 + bench.sector_read_bytes(3, 4) + 3 * bt * 2)
+    assert bench.algorithmic_bytes(inp, 4, 2) == want
+
+
+def test_kgb_bytes():
+    wl = ki.Workload("k", "packed", H=3, in_dtype="bf16", out_dtype="f32", seed=2, seqlens=(70, 5))
+    x = ki.build_kgb(wl, K=32)
+    rows = 75
+    assert bench.kgb_bytes(x, 2, 4) == rows * 3 * (32 * 2 + 32 * 4 + 2) + rows * 3 * 64 * 4
+
+
+def test_l2_flush_rule():
+    small = ki.build(ki.WORKLOADS["dense_1x64_h4_f32"])
+    assert bench.flushes_l2(small)
+    assert bench.workload_key(ki.WORKLOADS["packed_16x512_h64_f32"]) == "packed_16x512_h64_f32"
+    assert bench.workload_key(ki.WORKLOADS["packed_16x512_h64_f32"].with_(bt=16)) == "packed_16x512_h64_f32_bt16"
+
+
+CSV = '''==PROF== Connected to process 1
+"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"
+"0","1","python3.12","127.0.0.1","void kda_bt16_kernel<float, float>(SmallParams)","1","7","(64, 1, 1)","(2128, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","byte","33,569,792"
+"0","1","python3.12","127.0.0.1","void kda_bt16_kernel<float, float>(SmallParams)","1","7","(64, 1, 1)","(2128, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","Mbyte","0.07"
+"0","1","python3.12","127.0.0.1","void kda_bt16_kernel<float, float>(SmallParams)","1","7","(64, 1, 1)","(2128, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","ns","14944"
+'''
+
+
+def test_record_traffic(tmp_path, monkeypatch):
+    p = tmp_path / "t.csv"
+    p.write_text(CSV)
+    store = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_JSON", str(store))
+    e = bench.record_traffic(str(p), "w_bt16", "kda_bt16_kernel", "ncu ...")
+    assert e["dram_read"] == 33569792 and e["dram_write"] == 70000
+    assert e["dram_bytes_per_launch"] == 33639792
+    assert e["source_hash"] == bench.kernel_source_hash("kda_bt16_kernel")
+    assert json.load(open(store))["w_bt16"]["kda_bt16_kernel"] == e
+    # the record is used only while the kernel's sources are unchanged
+    assert bench.ncu_traffic("kda_bt16_kernel", "w_bt16") == 33639792
+    d = json.load(open(store))
+    d["w_bt16"]["kda_bt16_kernel"]["source_hash"] = "stale"
+    json.dump(d, open(store, "w"))
+    assert bench.ncu_traffic("kda_bt16_kernel", "w_bt16") is None
+
+
+def test_record_traffic_needs_one_launch(tmp_path):
+    lines = CSV.splitlines()
+    two = "\n".join(lines + [l.replace('"0","1","python', '"1","1","python') for l in lines[2:]])
+    p = tmp_path / "t.csv"
+    p.write_text(two)
+    with pytest.raises(ValueError):
+        bench.record_traffic(str(p), "w", "kda_bt16_kernel", "")
+
+
+def test_kernel_families_hash_their_own_sources():
+    a = bench.kernel_source_hash("kda_tril_kernel<MODE_FUSED>")
+    b = bench.kernel_source_hash("kda_bt16_kernel")
+    c = bench.kernel_source_hash("kda_kgb_kernel")
+    assert len({a, b, c}) == 3
+    assert bench.kernel_source_hash("kda_bt32_kernel") == b

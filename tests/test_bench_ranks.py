@@ -75,3 +75,15 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_fused_op():
+    """`bench.py --impl reference --op kgb`: the oracle of the fused path on the host."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--op", "kgb", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "packed_16x512_h64_f32_kgb"
+    assert d["config"]["key_dim"] == 128 and d["cpu_baseline"]["kind"] == "oracle"
