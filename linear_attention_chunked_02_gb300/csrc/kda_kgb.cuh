@@ -54,7 +54,9 @@ struct KgbParams {
 };
 
 constexpr int KGB_THREADS = 128;
-constexpr int KGB_SP = 36;                     // slice row pitch (floats): conflict-free fragments
+// slice row pitch (floats): the paired 8-byte fragment loads at 8 g + 2 t hit 32
+// distinct banks per half-warp
+constexpr int KGB_SP = 40;
 constexpr int KGB_SLICE = 64 * KGB_SP;         // floats per slice buffer
 constexpr int KGB_FLOATS = 2 * 4 * KGB_SLICE   // Q and P slices
                          + 4 * KGB_FROWS * 32  // f_IJ per slice and block pair, and a row of ones
@@ -176,19 +178,23 @@ __device__ __forceinline__ void kgb_block(const float *kq, const float *gp, cons
         const float *fs = fac + (s * KGB_FROWS + pr) * 32;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            const int d0 = 8 * ks + t, d1 = d0 + 4;
-            const float f0 = fs[d0], f1 = fs[d1];
+            // k-slots t and t + 4 of this k-step stand for channels 8 ks + 2t and 8 ks + 2t + 1
+            const int d0 = 8 * ks + 2 * t;
+            const float2 f = *reinterpret_cast<const float2 *>(fs + d0);
+            const float2 x0 = *reinterpret_cast<const float2 *>(q0 + d0);
+            const float2 x1 = *reinterpret_cast<const float2 *>(q1 + d0);
             uint32_t ah[4], al[4];
-            split_tf32(q0[d0] * f0, ah[0], al[0]);
-            split_tf32(q1[d0] * f0, ah[1], al[1]);
-            split_tf32(q0[d1] * f1, ah[2], al[2]);
-            split_tf32(q1[d1] * f1, ah[3], al[3]);
+            split_tf32(x0.x * f.x, ah[0], al[0]);
+            split_tf32(x1.x * f.x, ah[1], al[1]);
+            split_tf32(x0.y * f.y, ah[2], al[2]);
+            split_tf32(x1.y * f.y, ah[3], al[3]);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const float *pj = pb + 8 * nt * KGB_SP;
                 uint32_t bh0, bl0, bh1, bl1;
-                split_tf32(pj[d0], bh0, bl0);
-                split_tf32(pj[d1], bh1, bl1);
+                const float2 y = *reinterpret_cast<const float2 *>(pj + d0);
+                split_tf32(y.x, bh0, bl0);
+                split_tf32(y.y, bh1, bl1);
                 mma8(c.c[nt], al, bh0, bh1);
                 mma8(c.c[nt], ah, bl0, bl1);
                 mma8(c.c[nt], ah, bh0, bh1);
