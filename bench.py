@@ -478,6 +478,45 @@ def run_reference_kgb(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def copy_probe(nbytes: int = 134217728) -> dict:
+    """Pinned host <-> device copy rates of one GPU: each direction alone and both at
+    once on two streams (the floor of the end-to-end leg, which moves A in and Ai out)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def both():
+        cur = torch.cuda.current_stream()
+        s1.wait_stream(cur)
+        s2.wait_stream(cur)
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+        cur.wait_stream(s1)
+        cur.wait_stream(s2)
+
+    h2d = timed(lambda: d_in.copy_(h_in, non_blocking=True))
+    d2h = timed(lambda: h_out.copy_(d_out, non_blocking=True))
+    bi = timed(both)
+    return {"bytes_each_way": nbytes, "h2d_ms": h2d, "h2d_gbs": nbytes / h2d / 1e6, "d2h_ms": d2h,
+            "d2h_gbs": nbytes / d2h / 1e6, "both_ms": bi, "both_gbs_total": 2 * nbytes / bi / 1e6}
+
+
 def run_ours(args, world, rank, local):
     import linear_attention_chunked_02_gb300 as kda
     torch.cuda.set_device(local)
@@ -600,7 +639,12 @@ def main():
                     help="store the DRAM traffic of the launch captured in this ncu --csv log "
                          "for --workload/--bt in profiles/traffic.json, then exit")
     ap.add_argument("--ncu-command", default="", help="the command the capture ran (recorded)")
+    ap.add_argument("--copy-probe", action="store_true",
+                    help="print pinned host <-> device copy rates (the end-to-end floor) and exit")
     args = ap.parse_args()
+    if args.copy_probe:
+        print(json.dumps(copy_probe()))
+        return
     if args.record_traffic:
         wl = ki.WORKLOADS[args.workload].with_(bt=args.bt)
         key, kernel = ((f"{wl.name}_kgb", KGB_KERNEL) if args.op == "kgb" else (workload_key(wl), KERNEL[args.bt]))
