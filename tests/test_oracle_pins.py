@@ -177,6 +177,22 @@ def check_exact_64(orc):
         assert np.array_equal(orc.invert_chunk(M, BT), want), chain
 
 
+def check_similarity(orc):
+    """Power-of-two diagonal similarity: for D = diag(2^e), (I + D M D^-1)^-1 =
+    D (I + M)^-1 D^-1, exactly -- every term of row i, column j of the forward
+    substitution scales by the same 2^(e_i - e_j).  An index that takes a row or
+    column other than the term's own (M[i-1][k], X[k][j+1]) breaks it."""
+    rng = np.random.default_rng(17)
+    for n in (64, 37):
+        M = np.tril(rng.standard_normal((n, n)) * 0.2, -1)
+        e = rng.integers(-3, 4, n)
+        D = np.ldexp(1.0, e)
+        Ms = M * D[:, None] / D[None, :]
+        X = orc.invert_chunk(M, n)[:n, :n]
+        Xs = orc.invert_chunk(Ms, n)[:n, :n]
+        assert np.array_equal(Xs, X * D[:, None] / D[None, :]), n
+
+
 def check_residual(orc):
     """||(I + M) X - I||_max <= 1e-12 on config-style chunks, full and partial."""
     wl = ki.Workload("pin", "dense", H=3, in_dtype="f32", out_dtype="f32", seed=21, B=2, T=100)
@@ -343,7 +359,7 @@ KGB_CHECKS = [check_kgb_golden, check_kgb_nodecay, check_kgb_decay_closed_form,
               check_kgb_shift_invariance, check_kgb_generator]
 
 ALL_CHECKS = [check_golden, check_worked_small, check_rational, check_closed_form,
-              check_exact_64, check_residual, check_layout, check_poison] + KGB_CHECKS
+              check_exact_64, check_similarity, check_residual, check_layout, check_poison] + KGB_CHECKS
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
