@@ -39,6 +39,12 @@
  * calls are asynchronous on the given stream (a cudaStream_t passed as void*;
  * NULL = the legacy default stream) and do not synchronise the host.
  *
+ * Stream capture: the first call of each entry point on a device sets up
+ * per-device state (device attributes, the error word's address, kernel
+ * attributes and occupancy), so make it outside a CUDA-graph capture; later
+ * calls only encode tensor maps on the host and launch kernels, and can be
+ * captured.  kda_solve_tril_host also creates its copy streams on first use.
+ *
  * Errors: every function returns a kda_status_t.  Argument errors are found on
  * the host before any CUDA call and leave all buffers untouched.  KDA_ERR_CUDA
  * reports a launch failure (cudaGetLastError); faults during asynchronous
