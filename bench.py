@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -143,12 +144,20 @@ KERNEL_SOURCES = {"kda_tril_kernel": _COMMON_SOURCES, "kda_bt": _COMMON_SOURCES 
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed: what a traffic
+    capture depends on."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str) -> str:
     files = next(v for k, v in KERNEL_SOURCES.items() if kernel.startswith(k))
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_chunked_02_gb300", "csrc")
     for f in files:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

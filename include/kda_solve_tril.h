@@ -12,10 +12,10 @@
  *     Linv_ii = (I + A_ii)^-1,
  *     Linv_ij = -Linv_ii * sum_{k=j}^{i-1} A_ik * Linv_kj      (i > j).
  *
- * The same page says the shared solver's 64-token branch "supports both packed
- * and dense batch layouts" and selects "splitting by the FP32 workspace budget
- * and minimum input length; the workspace may use at most the FP32 input
- * size".  The split path runs the diagonal inverses as their own kernel and
+ * The same page says the shared solver's branch for 64-token chunks handles
+ * packed and dense batches, and that it decides whether to split from the FP32
+ * workspace budget and a minimum input length, the workspace being capped at
+ * the size of the input in FP32.  The split path runs the diagonal inverses as their own kernel and
  * keeps the four FP32 16x16 inverse tiles of every chunk-head in a caller
  * workspace; the single-pass path does everything on chip.  Both paths give
  * bit-identical results.
@@ -92,8 +92,8 @@ typedef enum {
     KDA_PATH_SINGLE = 2           /* one kernel, no workspace */
 } kda_path_t;
 
-/* Smallest B*T (total rows) for which the selector takes the split path
- * ("minimum input length", same PR description).  Set from GB300
+/* Smallest B*T (total rows) for which the selector takes the split path (the
+ * minimum input length of the same PR description).  Set from GB300
  * measurements: the single-pass kernel already inverts the four diagonal
  * blocks in parallel inside one CTA, so splitting only adds the workspace round
  * trip and a launch, and it was slower at every size measured (64 to 131072
@@ -113,8 +113,8 @@ KDA_API size_t kda_solve_tril_workspace_size(int64_t B, int64_t T, int32_t H, in
  * The path KDA_PATH_AUTO takes for this shape with a workspace of
  * workspace_bytes (0 = none): KDA_PATH_SPLIT iff the workspace is at least
  * kda_solve_tril_workspace_size(), that size is at most the FP32 input size
- * B*T*H*64*4 bytes (equivalently, chunks are on average at least 16 rows full,
- * "select by chunk occupancy to bound scratch") and B*T >= KDA_SPLIT_MIN_TOKENS;
+ * B*T*H*64*4 bytes (equivalently, chunks are on average at least 16 rows full:
+ * the choice rests on chunk occupancy) and B*T >= KDA_SPLIT_MIN_TOKENS;
  * KDA_PATH_SINGLE otherwise.  Pure host arithmetic.
  */
 KDA_API kda_path_t kda_solve_tril_select(int64_t B, int64_t T, int32_t H, int32_t num_seqs,
@@ -219,8 +219,8 @@ KDA_API kda_status_t kda_solve_tril_split_static(const void *A, void *Ai, const 
 
 /*
  * The same solve for chunks of bt = 16, 32 or 64 tokens.  The PR description
- * names the path it optimises the shared solver's "64-token branch"; the
- * solver's other branches invert (I + A) for the shorter chunk lengths, with A
+ * presents the path it optimises as the shared solver's branch for 64-token
+ * chunks; the solver's other branches invert (I + A) for shorter chunks, with A
  * the chunk's strictly lower-triangular bt x bt block:
  *
  *   bt = 16  one forward substitution per chunk-head (the 16x16 diagonal
@@ -248,7 +248,7 @@ KDA_API kda_status_t kda_solve_tril_bt(const void *A, void *Ai, const int32_t *c
 
 /*
  * The 64-token solve with the chunk matrix built on chip from the quantities
- * KDA prefill builds it from (the same page says KDA prefill opts into the
+ * KDA prefill builds it from (on the same page, KDA prefill is a user of the
  * shared solver):
  *
  *     A[i][j] = beta[i] * sum_d k[i][d] * k[j][d] * exp(g[i][d] - g[j][d])   (j < i),

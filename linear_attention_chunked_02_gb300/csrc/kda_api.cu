@@ -1,10 +1,10 @@
 // kda_api.cu -- C ABI of the KDA prefill chunk solver: argument checks, the
 // split / single-pass selector, TMA descriptors and kernel dispatch.
 //
-// The selector follows LightLLM PR #1703 (PR description): splitting is chosen
-// "by the FP32 workspace budget and minimum input length; the workspace may
-// use at most the FP32 input size", and the PR summary's "select by chunk
-// occupancy to bound scratch" -- the workspace is 4 KiB per chunk-head and the
+// The selector follows LightLLM PR #1703 (PR description and summary): the
+// split path is taken only when an FP32 workspace no larger than the FP32
+// input fits the caller's budget and the input is long enough, i.e. the choice
+// rests on how full the chunks are -- the workspace is 4 KiB per chunk-head and the
 // FP32 input is 256 B per row and head, so the budget holds exactly when
 // chunks are on average at least 16 rows full.
 #include <cuda.h>

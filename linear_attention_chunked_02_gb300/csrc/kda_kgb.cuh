@@ -1,8 +1,8 @@
 // kda_kgb.cuh -- KDA's chunk matrix built from keys, betas and decays, fused
 // with the 64-token solve: A never leaves shared memory.
 //
-// LightLLM PR #1703 (PR description) says KDA prefill opts into the shared
-// solver; the matrix it inverts is KDA's intra-chunk matrix
+// LightLLM PR #1703 (PR description) has KDA prefill use the shared solver;
+// the matrix it inverts is KDA's intra-chunk matrix
 //     A[i][j] = beta_i sum_d k_id k_jd exp(g_id - g_jd),   j < i,
 // with g the per-channel cumulative log decay.  Per chunk-head this kernel
 // builds the ten lower 16x16 blocks of A and solves (I + A)^-1 with the

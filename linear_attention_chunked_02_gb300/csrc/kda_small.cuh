@@ -1,7 +1,7 @@
 // kda_small.cuh -- the 32- and 16-token branches of the chunk solver.
 //
-// LightLLM PR #1703 (PR description) calls the path it optimises the shared
-// solver's "64-token branch"; the same inversion of (I + A) for the strictly
+// LightLLM PR #1703 (PR description) presents the path it optimises as the
+// shared solver's branch for 64-token chunks; the same inversion of (I + A) for the strictly
 // lower-triangular chunk matrix A is solved here for chunks of 16 and 32
 // tokens, with the same building blocks as the 64-token kernel:
 //   * 16 tokens: one 16-lane unit per chunk-head, forward substitution with one

@@ -20,19 +20,19 @@
  * valid rows.  Elements on or above the diagonal of A, and rows past n, are
  * never read.  Output row i (< n) is X[i][0..n) followed by 64 - n zeros.
  *
- * Chunk boundaries (readings of "packed and dense batch layouts" in the same
- * PR description): dense [B, T, H, 64] restarts chunks at t = 0 of every
+ * Chunk boundaries (readings of the packed and dense batches the same PR
+ * description supports): dense [B, T, H, 64] restarts chunks at t = 0 of every
  * batch row; packed [1, T, H, 64] with cu_seqlens restarts at every request
  * start cu_seqlens[s]; the last chunk of a row/request may be partial.
  *
- * The same page calls this the shared solver's "64-token branch", so the
- * chunk length is a parameter here (the _bt entry points; 16, 32 and 64 are
+ * The same page presents this as the shared solver's branch for 64-token
+ * chunks, so the chunk length is a parameter here (the _bt entry points; 16, 32 and 64 are
  * used): the definition above is unchanged with 64 replaced by the chunk
  * length bt.
  *
  * The chunk matrix itself (the _kgb entry point): KDA prefill builds A from the
  * keys k, the per-token betas and the per-channel cumulative log decays g of
- * the chunk's tokens, and the same page says KDA prefill opts into the shared
+ * the chunk's tokens, and on the same page KDA prefill is a user of the shared
  * solver.  The construction, written out as its definition with one exp per
  * term (no factorisation of the decay), is
  *

@@ -83,3 +83,11 @@ def test_kernel_families_hash_their_own_sources():
     c = bench.kernel_source_hash("kda_kgb_kernel")
     assert len({a, b, c}) == 3
     assert bench.kernel_source_hash("kda_bt32_kernel") == b
+
+
+def test_source_hash_ignores_comments_only():
+    a = "int f(int x) {  // add one\n    return x + 1; /* done */\n}\n"
+    b = "int f(int x) {\n    /* a different note */ return x + 1;\n}  // end\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)

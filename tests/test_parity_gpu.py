@@ -1,7 +1,7 @@
 """CUDA path vs the fp64 oracle, element by element, through the C ABI.
 
-Axes (LightLLM PR #1703 lists "packed layouts, dtypes, precision modes and
-fallback behavior" as its regression axes): layout {dense, packed} x input
+Axes (LightLLM PR #1703 regression-tests the layouts, the dtypes, the precision
+modes and the fallbacks): layout {dense, packed} x input
 dtype x output dtype x path {auto, split, single}, shape edges, the specified
 workloads at full size, exact structures, NaN poisoning of ignored elements,
 guard-band canaries, and bitwise equalities between paths and layouts.
