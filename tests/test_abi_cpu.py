@@ -188,3 +188,17 @@ def test_kgb_entry_no_gpu(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert call_kgb(L) == CUDA
+
+
+def test_python_binding_rejects_host_tensors_and_bad_shapes(L):
+    import torch
+    with pytest.raises(ValueError):
+        kda.solve_tril(torch.zeros(1, 64, 1, 64))                  # host tensor: no CPU path
+    with pytest.raises(ValueError):
+        kda.solve_tril_kgb(torch.zeros(1, 64, 1, 128), torch.zeros(1, 64, 1, 128), torch.zeros(1, 64, 1))
+    meta = torch.zeros(1, 64, 1, 48, device="meta")
+    with pytest.raises(ValueError):
+        kda._shape(meta, None, kda.CHUNK_LENGTHS)                  # chunk length 48 is not a branch
+    assert kda._shape(torch.zeros(2, 5, 3, 16, device="meta"), None, kda.CHUNK_LENGTHS) == (2, 5, 3, 0)
+    with pytest.raises(ValueError):
+        kda._shape(torch.zeros(2, 5, 3, 16, device="meta"), None)  # the 64-token entry points take 64 only
