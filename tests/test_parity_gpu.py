@@ -542,3 +542,57 @@ def test_small_chunks_specified_shapes(kda, orc, bt, name):
     out_dtype = ki.torch_dtype(wl.out_dtype)
     out, _ = solve(kda, inp, out_dtype, "single")
     check_large(orc, inp, out, out_dtype, f"{name} bt={bt}", full_limit=200000)
+
+
+# --------------------------------------- input guard bands and similarity
+
+def _nan_padded(t: torch.Tensor, pad: int = 4096) -> torch.Tensor:
+    """A device copy of t placed between NaN guard bands of `pad` elements."""
+    flat = torch.full((pad + t.numel() + pad,), float("nan"), dtype=t.dtype, device=DEV)
+    flat[pad:pad + t.numel()] = t.reshape(-1).to(DEV)
+    return flat[pad:pad + t.numel()].view(t.shape)
+
+
+@pytest.mark.parametrize("bt", [64, 32, 16])
+@pytest.mark.parametrize("layout", ["dense", "packed"])
+def test_inputs_between_nan_guard_bands(kda, bt, layout):
+    """Inputs sized exactly, NaN before and after: any read past the first or last
+    row would reach the output."""
+    kw = dict(B=2, T=3 * bt - 5) if layout == "dense" else dict(seqlens=(bt + 3, 1, 2 * bt - 1))
+    inp = ki.build(ki.Workload("guard", layout, H=3, in_dtype="bf16", out_dtype="f32", seed=bt, bt=bt,
+                               kind="gauss", **kw))
+    A, cu = to_dev(inp)
+    ref = kda.solve_tril(A, cu)
+    got = kda.solve_tril(_nan_padded(inp.A), cu)
+    torch.cuda.synchronize()
+    assert torch.equal(ref, got)
+    if bt == 64:
+        assert torch.equal(ref, kda.solve_tril(_nan_padded(inp.A), cu, path="split"))
+
+
+def test_kgb_inputs_between_nan_guard_bands(kda):
+    x = ki.build_kgb(ki.Workload("guard", "packed", H=3, in_dtype="bf16", out_dtype="f32", seed=6,
+                                 seqlens=(67, 1, 127)))
+    cu = x.cu_seqlens.to(DEV)
+    ref = kda.solve_tril_kgb(x.k.to(DEV), x.g.to(DEV), x.beta.to(DEV), cu)
+    got = kda.solve_tril_kgb(_nan_padded(x.k), _nan_padded(x.g), _nan_padded(x.beta), cu)
+    torch.cuda.synchronize()
+    assert torch.equal(ref, got)
+
+
+@pytest.mark.parametrize("bt", [64, 32, 16])
+def test_power_of_two_similarity_bitwise(kda, bt):
+    """D A D^-1 -> D Ai D^-1 bit for bit (D = diag(2^e) per chunk row): the split-TF32
+    products, the FP32 sums and the forward substitution all commute with scaling
+    by powers of two."""
+    inp = ki.build(ki.Workload("sim", "dense", H=2, in_dtype="f32", out_dtype="f32", seed=bt, B=1, T=2 * bt,
+                               kind="gauss", bt=bt))
+    e = torch.from_numpy(np.random.default_rng(bt).integers(-2, 3, bt)).double()
+    S = torch.pow(2.0, e[:, None] - e[None, :]).float()        # 2^(e_i - e_j), exact
+    A = inp.A.view(1, 2, bt, 2, bt)                           # [B, chunk, i, H, j]
+    As = (A * S[None, None, :, None, :]).reshape(inp.A.shape).contiguous()
+    paths = ("single", "split") if bt == 64 else ("auto",)
+    for path in paths:
+        X = kda.solve_tril(inp.A.to(DEV), path=path).cpu().view(1, 2, bt, 2, bt)
+        Xs = kda.solve_tril(As.to(DEV), path=path).cpu().view(1, 2, bt, 2, bt)
+        assert torch.equal(Xs, X * S[None, None, :, None, :]), path
