@@ -79,3 +79,28 @@ def residual_bound(M: np.ndarray, X: np.ndarray, out_dtype: torch.dtype) -> floa
     n = X.shape[0]
     L = np.eye(n) + np.tril(M[:n, :n], -1)
     return 1e-4 + float(np.abs(L).sum(1).max()) * 0.5 * float(ulp(X, out_dtype).max())
+
+
+def check_solution(got: np.ndarray, ref: np.ndarray, chunks, bt: int, in_dtype, out_dtype):
+    """Whole-output verdict.  got, ref: [rows, H, bt] fp64 (the output as computed and
+    the oracle's); chunks: (row0, n) of every chunk.  Rows in no chunk are not
+    compared; in the others the structural entries (diagonal, above it, columns at
+    or past n) must be equal exactly and every value finite and within bound().
+    Returns (ok, message)."""
+    rows = got.shape[0]
+    i_in = np.full(rows, -1)
+    for row0, n in chunks:
+        i_in[row0:row0 + n] = np.arange(n)
+    cov = i_in >= 0
+    got, ref, i_in = got[cov], ref[cov], i_in[cov]
+    struct = np.broadcast_to(np.arange(bt)[None, None, :] >= i_in[:, None, None], got.shape)
+    if not np.array_equal(got[struct], ref[struct]):
+        return False, "structural entries differ"
+    if not np.all(np.isfinite(got)):
+        return False, "non-finite output"
+    want, tol = bound(ref, in_dtype, out_dtype)
+    excess = np.abs(got - want) - tol
+    if excess.size and excess.max() > 0:
+        k = np.unravel_index(np.argmax(excess), excess.shape)
+        return False, f"max excess {excess.max():.3g} at {k}: got {got[k]!r} ref {ref[k]!r}"
+    return True, ""

@@ -57,22 +57,11 @@ def row_geometry(inp):
 
 
 def check_full(inp, got_t, ref, out_dtype, label=""):
-    """Vectorised comparison of every output element against the oracle."""
+    """Every output element against the oracle (oracle.parity.check_solution)."""
     H, bt = inp.H, inp.bt
     got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, bt)
-    ref = ref.reshape(-1, H, bt)
-    i_in, _ = row_geometry(inp)
-    covered = i_in >= 0
-    got, ref, i_in = got[covered], ref[covered], i_in[covered]
-    struct = np.arange(bt)[None, None, :] >= i_in[:, None, None]
-    struct = np.broadcast_to(struct, got.shape)
-    assert np.array_equal(got[struct], ref[struct]), f"{label}: structural entries differ"
-    assert np.all(np.isfinite(got)), f"{label}: non-finite output"
-    want, tol = parity.bound(ref, inp.A.dtype, out_dtype)
-    excess = np.abs(got - want) - tol
-    k = np.unravel_index(np.argmax(excess), excess.shape)
-    assert excess.max() <= 0, (f"{label}: max excess {excess.max():.3g} at {k}: got {got[k]!r} "
-                               f"ref {ref[k]!r}")
+    ok, msg = parity.check_solution(got, ref.reshape(-1, H, bt), inp.chunks(), bt, inp.A.dtype, out_dtype)
+    assert ok, f"{label}: {msg}"
 
 
 def check_residuals(inp, got_t, out_dtype, limit=2048, seed=0):

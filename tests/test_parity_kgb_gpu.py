@@ -52,22 +52,9 @@ def reference(orc, x, return_A=False):
 
 
 def check(x, got_t, ref, out_dtype, label):
-    H = x.H
-    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, H, 64)
-    ref = ref.reshape(-1, H, 64)
-    rows = x.B * x.T
-    i_in = np.full(rows, -1)
-    for row0, n in x.chunks():
-        i_in[row0:row0 + n] = np.arange(n)
-    cov = i_in >= 0
-    got, ref, i_in = got[cov], ref[cov], i_in[cov]
-    struct = np.broadcast_to(np.arange(64)[None, None, :] >= i_in[:, None, None], got.shape)
-    assert np.array_equal(got[struct], ref[struct]), f"{label}: structural entries differ"
-    assert np.all(np.isfinite(got)), f"{label}: non-finite output"
-    want, tol = parity.bound(ref, F32, out_dtype)
-    excess = np.abs(got - want) - tol
-    k = np.unravel_index(np.argmax(excess), excess.shape)
-    assert excess.max() <= 0, f"{label}: max excess {excess.max():.3g} at {k}: got {got[k]!r} ref {ref[k]!r}"
+    got = got_t.to(torch.float64).cpu().numpy().reshape(-1, x.H, 64)
+    ok, msg = parity.check_solution(got, ref.reshape(-1, x.H, 64), x.chunks(), 64, F32, out_dtype)
+    assert ok, f"{label}: {msg}"
 
 
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 33, 63, 64, 65, 130])
