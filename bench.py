@@ -188,8 +188,12 @@ _UNIT = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1
 
 
 def record_traffic(csv_path: str, workload: str, kernel: str, command: str) -> dict:
-    """Store the DRAM bytes of the one captured launch in an ncu --csv log (metrics
-    dram__bytes_read.sum and dram__bytes_write.sum) under (workload, kernel)."""
+    """Store the per-launch DRAM bytes of the launches captured in an ncu --csv log
+    (metrics dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum)
+    under (workload, kernel): the mean over the captured launches.  Captured as
+    consecutive launches with --cache-control none, each launch's write figure
+    includes the previous launch's output lines that it evicts from L2, so in the
+    steady state the mean is the whole per-launch traffic."""
     import csv
     with open(csv_path) as f:
         lines = [ln for ln in f if ln.startswith('"')]
@@ -199,14 +203,17 @@ def record_traffic(csv_path: str, workload: str, kernel: str, command: str) -> d
         if name in ("dram__bytes_read.sum", "dram__bytes_write.sum", "gpu__time_duration.sum"):
             v = float(r["Metric Value"].replace(",", ""))
             vals.setdefault(r["ID"], {})[name] = v * _UNIT.get(r.get("Metric Unit", "byte"), 1.0)
-    if len(vals) != 1:
-        raise ValueError(f"expected one captured launch in {csv_path}, found {len(vals)}")
-    m = next(iter(vals.values()))
+    if not vals:
+        raise ValueError(f"no captured launch in {csv_path}")
+    n = len(vals)
+    mean = {k: sum(v[k] for v in vals.values()) / n
+            for k in ("dram__bytes_read.sum", "dram__bytes_write.sum", "gpu__time_duration.sum")}
+    rd, wr, ns = mean["dram__bytes_read.sum"], mean["dram__bytes_write.sum"], mean["gpu__time_duration.sum"]
     entry = {"source_hash": kernel_source_hash(kernel),
-             "dram_bytes_per_launch": int(m["dram__bytes_read.sum"] + m["dram__bytes_write.sum"]),
-             "dram_read": int(m["dram__bytes_read.sum"]), "dram_write": int(m["dram__bytes_write.sum"]),
-             "note": f"one ncu launch capture: {command}; output lines still dirty in L2 at kernel "
-                     "end are not in the write figure"}
+             "dram_bytes_per_launch": int(rd + wr), "dram_read": int(rd), "dram_write": int(wr),
+             "launches": n, "ncu_us_per_launch": ns / 1e3,
+             "physical_gbs": (rd + wr) / ns,
+             "note": f"mean over {n} consecutive launches: {command}"}
     try:
         d = json.load(open(TRAFFIC_JSON))
     except (OSError, ValueError):

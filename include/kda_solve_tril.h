@@ -42,8 +42,12 @@
  * Stream capture: the first call of each entry point on a device sets up
  * per-device state (device attributes, the error word's address, kernel
  * attributes and occupancy), so make it outside a CUDA-graph capture; later
- * calls only encode tensor maps on the host and launch kernels, and can be
- * captured.  kda_solve_tril_host also creates its copy streams on first use.
+ * calls only encode tensor maps on the host (the last 16 distinct (A, Ai,
+ * dtypes, H, rows) encodings are kept and reused) and launch kernels, and can
+ * be captured.  kda_solve_tril_host also creates its copy streams on first use.
+ * That per-device state lives until the process exits and does not survive a
+ * cudaDeviceReset (or anything else that destroys the device's primary
+ * context): after one, do not call the library on that device again.
  *
  * Errors: every function returns a kda_status_t.  Argument errors are found on
  * the host before any CUDA call and leave all buffers untouched.  KDA_ERR_CUDA
@@ -199,10 +203,11 @@ KDA_API kda_status_t kda_solve_tril_host(const void *A_host, void *Ai_host, cons
  * workspace is a static device array of KDA_STATIC_WS_BYTES (64 MiB) inside the
  * library, held by every GPU that loads the library until the process exits.
  *
- *   - Shapes whose workspace (kda_solve_tril_workspace_size) exceeds
- *     KDA_STATIC_WS_BYTES are rejected with KDA_ERR_WORKSPACE before any CUDA
- *     call; 64 MiB holds 16384 chunk-heads, e.g. the 16 x 512-token, 64-head
- *     packed solve (35.75 MiB).
+ *   - Argument errors (those of kda_solve_tril) are reported before any CUDA
+ *     call.  Shapes whose workspace (kda_solve_tril_workspace_size) exceeds
+ *     KDA_STATIC_WS_BYTES are rejected with KDA_ERR_WORKSPACE, also before any
+ *     CUDA call; 64 MiB holds 16384 chunk-heads, e.g. the 16 x 512-token,
+ *     64-head packed solve (35.75 MiB).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
@@ -259,9 +264,11 @@ KDA_API kda_status_t kda_solve_tril_bt(const void *A, void *Ai, const int32_t *c
  *   k           device, [B, T, H, K] of in_dtype (keys), 16-byte aligned.
  *   g           device, [B, T, H, K] float32: per-channel cumulative log decay;
  *               only differences inside a chunk are used, so g may restart at
- *               chunk starts or run on.  16-byte aligned.  Within any 16-token
- *               block of a chunk, g may fall by at most 80 per channel (larger
- *               drops overflow FP32 and give non-finite results).
+ *               chunk starts or run on.  16-byte aligned.  g must not increase
+ *               along a chunk (each token's decay is at most 1); how far it
+ *               falls is not limited.  Channels that fall by more than 32
+ *               within a 16-token block take a slower path for that block
+ *               (KDA's decays, about one per token, do not).
  *   beta        device, [B, T, H] of in_dtype, aligned to its element size.
  *   Ai          device, [B, T, H, 64] of out_dtype, 16-byte aligned; must not
  *               overlap k, g or beta.

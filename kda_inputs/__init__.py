@@ -36,6 +36,14 @@ that dropped them would still pass a tolerance test on KDA-style inputs:
 
 * ``"nodecay"``: the same construction with ``g == 0``;
 * ``"gauss"``: ``A[t, h, j] ~ N(0, 0.2^2)`` for ``j < i``, 0 otherwise.
+
+A third kind, ``"steep"``, exists only for the keys/decays/betas inputs
+(``build_kgb``): KDA's decay may fall steeply, and a construction that factors
+``exp(g_i - g_j)`` through a reference row can overflow or lose the large terms
+there.  Per channel ``d`` the per-token drop of ``g`` is, by ``d mod 4``:
+0: uniform in [8, 20] nats; 1: the KDA drop plus, with probability 1/16 per
+token, a cliff of 100 nats; 2: uniform in [3, 8] nats; 3: the KDA drop.  The
+extra uniforms are drawn after the ``g`` pre-activations of each slab.
 """
 from __future__ import annotations
 
@@ -65,7 +73,7 @@ class Workload:
     T: int = 0                       # dense: tokens per batch row
     seqlens: Optional[Sequence[int]] = None   # packed: fixed request lengths
     ragged: Optional[tuple] = None   # packed: (num_requests, min_len, max_len) drawn from the seed
-    kind: str = "kda"                # "kda" | "nodecay" | "gauss"
+    kind: str = "kda"                # "kda" | "nodecay" | "gauss" | "steep" (build_kgb only)
     bt: int = BT                     # chunk length (64, or the 32 / 16 branches)
 
     def with_(self, **kw) -> "Workload":
@@ -149,11 +157,18 @@ def _draw_kgb(rng: np.random.Generator, L: int, H: int, kind: str, bt: int = BT,
     k /= np.linalg.norm(k, axis=-1, keepdims=True)
     beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((L, H))))
     gpre = rng.standard_normal((L, H, K))
+    pad = ((0, Lp - L), (0, 0), (0, 0))
     if kind == "nodecay":
         g = np.zeros_like(k)
-    elif kind == "kda":
-        pad = ((0, Lp - L), (0, 0), (0, 0))
-        g = np.cumsum(-_softplus(np.pad(gpre, pad)).reshape(C, bt, H, K), axis=1).reshape(Lp, H, K)[:L]
+    elif kind in ("kda", "steep"):
+        drop = _softplus(gpre)
+        if kind == "steep":
+            u = rng.random((L, H, K))
+            cls = np.arange(K) % 4
+            drop = np.where(cls == 0, 8.0 + 12.0 * u,
+                            np.where(cls == 1, drop + 100.0 * (u < 1.0 / 16.0),
+                                     np.where(cls == 2, 3.0 + 5.0 * u, drop)))
+        g = np.cumsum(-np.pad(drop, pad).reshape(C, bt, H, K), axis=1).reshape(Lp, H, K)[:L]
     else:
         raise ValueError(f"unknown input kind {kind!r}")
     return k, beta, g
@@ -170,6 +185,8 @@ def _slab(rng: np.random.Generator, L: int, H: int, kind: str, bt: int = BT) -> 
         vals = np.concatenate([vals, np.zeros((Lp - L, H, bt))], axis=0)
         S = vals.reshape(C, bt, H, bt)                       # [C, i, H, j]
         keep = (col < row)[None, :, None, :]
+    elif kind == "steep":
+        raise ValueError("the steep kind is defined for build_kgb only")
     else:
         k, beta, g = _draw_kgb(rng, L, H, kind, bt)
         pad = ((0, Lp - L), (0, 0), (0, 0))
@@ -266,7 +283,7 @@ class KgbInput:
 
 
 def build_kgb(wl: Workload, K: int = KEY_DIM) -> KgbInput:
-    """Seeded (k, g, beta) for ``wl`` (kinds "kda" and "nodecay"), drawn exactly as
+    """Seeded (k, g, beta) for ``wl`` (kinds "kda", "nodecay" and "steep"), drawn exactly as
     for ``build``: with K = 128 and the same workload, the chunk matrices built from
     them by the KDA construction are the ``A`` that ``build`` returns (before rounding)."""
     if wl.kind == "gauss":

@@ -41,7 +41,7 @@ def _stale(out: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Build (if stale) and return the path of the shared library."""
     os.makedirs(BUILD, exist_ok=True)
-    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "kda_solve_tril.h"))
     cc = nvcc()
     jobs = []

@@ -16,6 +16,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "kda_internal.h"
 #include "kda_launch.cuh"
 #include "kda_solve_tril.h"
 
@@ -102,6 +103,41 @@ bool make_maps(const void *A, int32_t in_dt, void *Ai, int32_t out_dt, int32_t H
     return encode_maps(A, in_dt, H, rows, maps.m, 4) && encode_maps(Ai, out_dt, H, rows, maps.o, 3);
 }
 
+// Encoded tensor maps of recent calls, keyed by everything they encode (base
+// addresses, dtypes, H, rows): a map is a pure function of its key, so a hit is
+// exact even if the caller's buffers were freed and reallocated meanwhile.
+// Saves the seven encodings on the host for repeated solves on the same buffers.
+struct MapKey {
+    const void *A, *Ai;
+    int32_t in_dt, out_dt, H;
+    int64_t rows;
+    bool operator==(const MapKey &o) const {
+        return A == o.A && Ai == o.Ai && in_dt == o.in_dt && out_dt == o.out_dt && H == o.H && rows == o.rows;
+    }
+};
+constexpr int kMapCache = 16;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCache];
+kda::Maps g_map_val[kMapCache];
+int g_map_n = 0, g_map_next = 0;
+
+bool cached_maps(const void *A, int32_t in_dt, void *Ai, int32_t out_dt, int32_t H, int64_t rows, kda::Maps &maps) {
+    const MapKey key{A, Ai, in_dt, out_dt, H, rows};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_map_n; ++i)
+        if (g_map_key[i] == key) {
+            maps = g_map_val[i];
+            return true;
+        }
+    std::memset(&maps, 0, sizeof(maps));
+    if (!make_maps(A, in_dt, Ai, out_dt, H, rows, maps)) return false;
+    g_map_key[g_map_next] = key;
+    g_map_val[g_map_next] = maps;
+    g_map_next = (g_map_next + 1) % kMapCache;
+    if (g_map_n < kMapCache) ++g_map_n;
+    return true;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
@@ -162,6 +198,20 @@ cudaError_t copy_engines(int device, CopyEngines *&ce) {
 
 }  // namespace
 
+namespace kda {
+
+kda_status_t validate_solve(const void *A, const void *Ai, const int32_t *cu, int32_t num_seqs, int64_t B,
+                            int64_t T, int32_t H, int32_t in_dt, int32_t out_dt) {
+    const kda_status_t st = check_args(A, Ai, cu, num_seqs, B, T, H, in_dt, out_dt);
+    if (st != KDA_OK || B == 0 || T == 0) return st;
+    const size_t elems = size_t(B) * size_t(T) * size_t(H) * BT;
+    if (!aligned16(A) || !aligned16(Ai)) return KDA_ERR_INVALID_ARGUMENT;
+    if (overlaps(A, elems * elt_size(in_dt), Ai, elems * elt_size(out_dt))) return KDA_ERR_INVALID_ARGUMENT;
+    return KDA_OK;
+}
+
+}  // namespace kda
+
 extern "C" {
 
 size_t kda_solve_tril_workspace_size(int64_t B, int64_t T, int32_t H, int32_t num_seqs) {
@@ -214,9 +264,8 @@ kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *cu_seqlen
     if (device_info(device, info) != cudaSuccess) return KDA_ERR_CUDA;
 
     kda::Maps maps;
-    std::memset(&maps, 0, sizeof(maps));
     const int64_t rows = B * T;
-    if (!make_maps(A, in_dtype, Ai, out_dtype, H, rows, maps)) return KDA_ERR_CUDA;
+    if (!cached_maps(A, in_dtype, Ai, out_dtype, H, rows, maps)) return KDA_ERR_CUDA;
 
     kda::Params p;
     p.out = Ai;

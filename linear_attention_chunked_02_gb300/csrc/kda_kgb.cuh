@@ -8,15 +8,19 @@
 // builds the ten lower 16x16 blocks of A and solves (I + A)^-1 with the
 // 64-token kernel's schedule.
 //
-// Construction.  For block (I, J), I >= J, with reference rows rI = 16 I and
-// rJ = 16 J:
+// Construction.  Block I of the chunk has first row rI = 16 I and last live
+// row eI = min(16 I + 15, n - 1).  For block (I, J), I >= J:
 //     A_IJ = (Q_I * f_IJ) P_J^T,  Q_I[i][d] = k_id exp(g_id - g_rI,d),
-//     P_J[j][d] = k_jd exp(g_rJ,d - g_jd),  f_IJ[d] = exp(g_rI,d - g_rJ,d),
-// where every exponent of Q and f is <= 0 when the decays are non-positive,
-// and the exponents of P span at most the 15 tokens after rJ (the inputs must
-// keep that below 80 nats per channel, or P overflows).  The products run
-// on the tensor cores in split TF32 (mma.sync m16n8k8, hi/lo parts, FP32
-// accumulation).
+//     P_J[j][d] = k_jd exp(g_eJ,d - g_jd),  f_IJ[d] = exp(g_rI,d - g_eJ,d).
+// g is non-increasing along the chunk (a cumulative log decay), so every
+// exponent of Q and P is <= 0, and so is f's for I > J: none of these factors
+// can overflow, and one that underflows stands for a term below FP32's range.
+// Only the diagonal factor f_II = exp(span) with span = g_rI - g_eI >= 0
+// grows: channels whose span exceeds KGB_SAFE_SPAN get f_II = 0, and their
+// terms k_id k_jd exp(g_id - g_jd) are added to the diagonal block one by one
+// (a slow path that KDA's ordinary decays, about 1 nat per token, never take).
+// The products run on the tensor cores in split TF32 (mma.sync m16n8k8, hi/lo
+// parts, FP32 accumulation).
 //
 // Work split (one persistent CTA of 128 threads per resident slot, one
 // chunk-head at a time):
@@ -36,8 +40,11 @@
 
 namespace kda {
 
-// factor rows per slice: the six block pairs I > J, then a row of ones (I == J)
-constexpr int KGB_FROWS = 7;
+// factor rows per slice: the six block pairs I > J, then the four diagonal blocks
+constexpr int KGB_FROWS = 10;
+// largest decay (nats) over a diagonal block that its tensor-core product takes,
+// in log2 units; steeper channels go through the slow path
+constexpr float KGB_SAFE_SPAN2 = 32.0f * 1.4426950408889634f;
 
 struct KgbParams {
     const void *k;             // [rows, H, K], input dtype
@@ -59,10 +66,11 @@ constexpr int KGB_THREADS = 128;
 constexpr int KGB_SP = 40;
 constexpr int KGB_SLICE = 64 * KGB_SP;         // floats per slice buffer
 constexpr int KGB_FLOATS = 2 * 4 * KGB_SLICE   // Q and P slices
-                         + 4 * KGB_FROWS * 32  // f_IJ per slice and block pair, and a row of ones
+                         + 4 * KGB_FROWS * 32  // f_IJ per slice, block pair and diagonal block
                          + 10 * 256            // A blocks, pitch 16
                          + 4 * XTS + 4 * XRS   // inverse tiles of the merge
-                         + 64;                 // beta of the chunk's rows
+                         + 64                  // beta of the chunk's rows
+                         + 16;                 // steep-channel masks [slice][diagonal block]
 constexpr int KGB_BYTES = KGB_FLOATS * 4;
 
 __device__ __forceinline__ void named_sync64() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
@@ -127,20 +135,33 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 template <typename TIn>
-__device__ __forceinline__ void kgb_transform(float *kb, float *gb, float *fac, int n, int d) {
-    // f_IJ = exp(g_rI - g_rJ), I > J (zero when block I starts past the chunk's end)
+__device__ __forceinline__ void kgb_transform(float *kb, float *gb, float *fac, unsigned *steep, int n, int d) {
     // exponents are differences of g taken first (exact for nearby values), then
     // scaled to base 2, so their error does not grow with |g|
     constexpr float LOG2E = 1.4426950408889634f;
-    float gr[4];
+    float gr[4], ge[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) gr[b] = gb[16 * b * KGB_SP + d];
+    for (int b = 0; b < 4; ++b) {
+        const int e = 16 * b + 15 < n ? 16 * b + 15 : n - 1;
+        gr[b] = gb[16 * b * KGB_SP + d];
+        ge[b] = gb[(e > 0 ? e : 0) * KGB_SP + d];
+    }
+    // f_IJ = exp(g_rI - g_eJ), I > J (zero when block I starts past the chunk's end)
 #pragma unroll
     for (int I = 1; I < 4; ++I)
 #pragma unroll
         for (int J = 0; J < I; ++J)
-            fac[(I * (I - 1) / 2 + J) * 32 + d] = 16 * I < n ? ex2((gr[I] - gr[J]) * LOG2E) : 0.f;
-    fac[6 * 32 + d] = 1.f;
+            fac[(I * (I - 1) / 2 + J) * 32 + d] = 16 * I < n ? ex2((gr[I] - ge[J]) * LOG2E) : 0.f;
+    // f_II = exp(g_rI - g_eI), zero for a channel that falls further than the
+    // safe span over the block (its terms take the slow path)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const float span = (gr[b] - ge[b]) * LOG2E;
+        const bool live = 16 * b < n, st = live && !(span <= KGB_SAFE_SPAN2);
+        fac[(6 + b) * 32 + d] = live && !st ? ex2(span) : 0.f;
+        const unsigned m = __ballot_sync(0xffffffffu, st);
+        if (d == 0) steep[b] = m;
+    }
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         float kv[16];
@@ -158,19 +179,67 @@ __device__ __forceinline__ void kgb_transform(float *kb, float *gb, float *fac, 
         for (int i = 0; i < 16; ++i) {
             const int r = 16 * b + i;
             const bool live = r < n;
-            const float e = (gb[r * KGB_SP + d] - gr[b]) * LOG2E;
-            kb[r * KGB_SP + d] = live ? kv[i] * ex2(e) : 0.f;
-            gb[r * KGB_SP + d] = live ? kv[i] * ex2(-e) : 0.f;
+            const float gv = gb[r * KGB_SP + d];
+            kb[r * KGB_SP + d] = live ? kv[i] * ex2((gv - gr[b]) * LOG2E) : 0.f;    // Q
+            gb[r * KGB_SP + d] = live ? kv[i] * ex2((ge[b] - gv) * LOG2E) : 0.f;    // P
+        }
+    }
+}
+
+// Slow path of diagonal block I: the terms of the channels in the steep masks,
+// k_id k_jd exp(g_id - g_jd) one by one, read again from global memory, added to
+// the lane's C fragments (rows g, g + 8; columns 8 nt + 2 t + e).
+template <typename TIn>
+__device__ __forceinline__ void kgb_steep_terms(const KgbParams &p, const Meta &m, const unsigned *steep, int I,
+                                             int nsl, int g, int t, TileC &c) {
+    constexpr float LOG2E = 1.4426950408889634f;
+    const int64_t rs = int64_t(p.H) * p.K;
+    const int64_t base = (int64_t(m.row0) + 16 * I) * rs + int64_t(m.h) * p.K;
+    const TIn *kp = reinterpret_cast<const TIn *>(p.k) + base;
+    const float *gp = p.g + base;
+    const int li[2] = {g, g + 8};
+    const int lj[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+    for (int s = 0; s < nsl; ++s) {
+        unsigned mask = steep[s * 4 + I];
+        while (mask != 0u) {
+            const int d = 32 * s + __ffs(mask) - 1;
+            mask &= mask - 1u;
+            float ki[2], gi[2], kj[4], gj[4];
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+                const bool live = 16 * I + li[a] < m.n;
+                ki[a] = live ? float(kp[li[a] * rs + d]) : 0.f;
+                gi[a] = live ? gp[li[a] * rs + d] : 0.f;
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const bool live = 16 * I + lj[a] < m.n;
+                kj[a] = live ? float(kp[lj[a] * rs + d]) : 0.f;
+                gj[a] = live ? gp[lj[a] * rs + d] : 0.f;
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int a = 2 * nt + e;
+                        if (lj[a] < li[h])      // strictly lower; dead rows hold k = 0
+                            c.c[nt][2 * h + e] = fmaf(ki[h] * kj[a], ex2((gi[h] - gj[a]) * LOG2E), c.c[nt][2 * h + e]);
+                    }
         }
     }
 }
 
 // Block (I, J) of A over all nsl slices, times beta, masked, into Ab (pitch 16).
-__device__ __forceinline__ void kgb_block(const float *kq, const float *gp, const float *fac, const float *bs,
-                                          float *Ab, int I, int J, int nsl, int n, int g, int t) {
+template <typename TIn>
+__device__ __forceinline__ void kgb_block(const KgbParams &p, const Meta &m, const float *kq, const float *gp,
+                                          const float *fac, const unsigned *steep, const float *bs, float *Ab,
+                                          int I, int J, int nsl, int g, int t) {
+    const int n = m.n;
     TileC c;
     zero(c);
-    const int pr = I > J ? I * (I - 1) / 2 + J : 6;       // 6: the row of ones
+    const int pr = I > J ? I * (I - 1) / 2 + J : 6 + I;
     for (int s = 0; s < nsl; ++s) {
         const float *q0 = kq + s * KGB_SLICE + (16 * I + g) * KGB_SP;
         const float *q1 = q0 + 8 * KGB_SP;
@@ -200,6 +269,11 @@ __device__ __forceinline__ void kgb_block(const float *kq, const float *gp, cons
                 mma8(c.c[nt], ah, bh0, bh1);
             }
         }
+    }
+    if (I == J) {
+        unsigned any = 0u;
+        for (int s = 0; s < nsl; ++s) any |= steep[s * 4 + I];
+        if (any != 0u) kgb_steep_terms<TIn>(p, m, steep, I, nsl, g, t, c);
     }
     // C fragments: c[nt][2 h + e] = block row g + 8 h, block column 8 nt + 2 t + e
     float *Ad = Ab + blk(I, J) * 256;
@@ -316,6 +390,7 @@ kda_kgb_kernel(const KgbParams p) {
     float *Xt = Ab + 10 * 256;
     float *Xr = Xt + 4 * XTS;
     float *bs = Xr + 4 * XRS;
+    unsigned *steep = reinterpret_cast<unsigned *>(bs + 64);     // [slice][diagonal block]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int nsl = p.K / 32;
@@ -339,7 +414,7 @@ kda_kgb_kernel(const KgbParams p) {
         }
         cp_async_wait<0>();
         __syncwarp();
-        if (has_slice) kgb_transform<TIn>(kb, gb, fac + warp * KGB_FROWS * 32, cur.n, lane);
+        if (has_slice) kgb_transform<TIn>(kb, gb, fac + warp * KGB_FROWS * 32, steep + 4 * warp, cur.n, lane);
         if (warp == 0) {
             bs[lane] = b0;
             bs[lane + 32] = b1;
@@ -350,7 +425,7 @@ kda_kgb_kernel(const KgbParams p) {
         for (int b = warp; b < 10; b += 4) {
             const int I = b >= 6 ? 3 : b >= 3 ? 2 : b >= 1 ? 1 : 0;
             const int J = b - I * (I + 1) / 2;
-            kgb_block(kq, gp, fac, bs, Ab, I, J, nsl, cur.n, g, t);
+            kgb_block<TIn>(p, cur, kq, gp, fac, steep, bs, Ab, I, J, nsl, g, t);
         }
         __syncthreads();                               // A complete; the slice buffers are free
         const Meta nxt = walk.next(p);

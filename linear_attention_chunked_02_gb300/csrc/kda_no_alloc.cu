@@ -13,6 +13,7 @@
 
 #include <mutex>
 
+#include "kda_internal.h"
 #include "kda_solve_tril.h"
 
 namespace {
@@ -21,7 +22,9 @@ namespace {
 // for the device array: its device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_kda_static_ws[KDA_STATIC_WS_BYTES];
 
-// Device address of g_kda_static_ws per device, resolved once per device.
+// Device address of g_kda_static_ws per device, resolved once per device (a
+// cudaDeviceReset of that device would make it stale: the library's per-device
+// state does not survive one).
 cudaError_t static_ws_ptr(void **out) {
     static std::mutex mu;
     static void *ptrs[64] = {nullptr};
@@ -45,8 +48,12 @@ cudaError_t static_ws_ptr(void **out) {
 extern "C" kda_status_t kda_solve_tril_split_static(const void *A, void *Ai, const int32_t *cu_seqlens,
                                                     int32_t num_seqs, int64_t B, int64_t T, int32_t H,
                                                     int32_t in_dtype, int32_t out_dtype, void *stream) {
+    // every argument error is reported before any CUDA call
+    const kda_status_t st = kda::validate_solve(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype);
+    if (st != KDA_OK) return st;
     const size_t need = kda_solve_tril_workspace_size(B, T, H, num_seqs);
     if (need > size_t(KDA_STATIC_WS_BYTES)) return KDA_ERR_WORKSPACE;
+    if (B == 0 || T == 0) return KDA_OK;
     void *ws = nullptr;
     if (static_ws_ptr(&ws) != cudaSuccess) return KDA_ERR_CUDA;
     // Nothing in the array needs to start at zero: the diagonal-inverse kernel

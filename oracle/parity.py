@@ -104,3 +104,35 @@ def check_solution(got: np.ndarray, ref: np.ndarray, chunks, bt: int, in_dtype, 
         k = np.unravel_index(np.argmax(excess), excess.shape)
         return False, f"max excess {excess.max():.3g} at {k}: got {got[k]!r} ref {ref[k]!r}"
     return True, ""
+
+
+def parts(inp, limit: int):
+    """Independent parts of a solver input (a kda_inputs.SolverInput), each of at
+    most `limit` chunk-heads where the layout allows: whole batch rows (dense) or
+    whole requests (packed), so that the fp64 reference of one part fits in host
+    memory.  Yields (first row, row count, A of the part, its cu_seqlens or None,
+    its chunks as (row0, n) relative to the part)."""
+    H, bt = inp.H, inp.bt
+    chunks = inp.chunks()
+    if inp.cu_seqlens is None:
+        per_row = -(-inp.T // bt) * H if inp.T > 0 else 1
+        step = max(1, limit // per_row)
+        for b0 in range(0, inp.B, step):
+            b1 = min(inp.B, b0 + step)
+            lo, hi = b0 * inp.T, b1 * inp.T
+            yield lo, hi - lo, inp.A[b0:b1], None, [(r0 - lo, n) for (r0, n) in chunks if lo <= r0 < hi]
+        return
+    cu = inp.cu_seqlens.tolist()
+    s0 = 0
+    while s0 < len(cu) - 1:
+        s1, tasks = s0, 0
+        while s1 < len(cu) - 1:
+            t = -(-(cu[s1 + 1] - cu[s1]) // bt) * H
+            if s1 > s0 and tasks + t > limit:
+                break
+            tasks += t
+            s1 += 1
+        lo, hi = cu[s0], cu[s1]
+        sub_cu = torch.tensor([c - lo for c in cu[s0:s1 + 1]], dtype=torch.int32)
+        yield lo, hi - lo, inp.A[:, lo:hi], sub_cu, [(r0 - lo, n) for (r0, n) in chunks if lo <= r0 < hi]
+        s0 = s1

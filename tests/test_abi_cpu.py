@@ -98,6 +98,28 @@ def test_argument_errors_before_any_cuda_call(L):
     assert st == OK
 
 
+def call_static(L, A=16, Ai=1 << 20, cu=None, nseq=0, B=1, T=64, H=1, ind=0, outd=0):
+    return L.kda_solve_tril_split_static(A, Ai, cu, nseq, B, T, H, ind, outd, None)
+
+
+def test_static_entry_argument_errors_before_any_cuda_call(L):
+    """kda_solve_tril_split_static reports argument errors itself, before it looks
+    up its built-in workspace: without a GPU, any CUDA call would give KDA_ERR_CUDA."""
+    assert call_static(L, ind=7) == UNSUPPORTED
+    assert call_static(L, outd=3) == UNSUPPORTED
+    assert call_static(L, H=0) == INVALID
+    assert call_static(L, A=None) == INVALID
+    assert call_static(L, Ai=None) == INVALID
+    assert call_static(L, A=8) == INVALID                      # misaligned
+    assert call_static(L, A=1 << 20, Ai=(1 << 20) + 4096) == INVALID
+    assert call_static(L, cu=4096, nseq=1, B=2) == INVALID     # packed needs B == 1
+    assert call_static(L, cu=None, nseq=2) == INVALID
+    assert call_static(L, T=1 << 31) == UNSUPPORTED
+    assert call_static(L, A=1 << 40, Ai=1 << 44, T=1 << 20, H=64) == WORKSPACE   # beyond the built-in 64 MiB
+    assert call_static(L, T=0) == OK
+    assert call_static(L, B=0) == OK
+
+
 def test_status_strings(L):
     for s in range(6):
         assert L.kda_status_string(s)

@@ -68,11 +68,24 @@ def test_record_traffic(tmp_path, monkeypatch):
     assert bench.ncu_traffic("kda_bt16_kernel", "w_bt16") is None
 
 
-def test_record_traffic_needs_one_launch(tmp_path):
+def test_record_traffic_averages_consecutive_launches(tmp_path, monkeypatch):
+    """Several consecutive launches: the record is their mean per launch."""
     lines = CSV.splitlines()
-    two = "\n".join(lines + [l.replace('"0","1","python', '"1","1","python') for l in lines[2:]])
+    second = [l.replace('"0","1","python', '"1","1","python').replace('"33,569,792"', '"33,569,800"')
+              .replace('"0.07"', '"0.09"').replace('"14944"', '"14956"') for l in lines[2:]]
     p = tmp_path / "t.csv"
-    p.write_text(two)
+    p.write_text("\n".join(lines + second))
+    monkeypatch.setattr(bench, "TRAFFIC_JSON", str(tmp_path / "traffic.json"))
+    e = bench.record_traffic(str(p), "w", "kda_bt16_kernel", "ncu ...")
+    assert e["launches"] == 2
+    assert e["dram_read"] == 33569796 and e["dram_write"] == 80000
+    assert abs(e["ncu_us_per_launch"] - 14.95) < 1e-9
+    assert abs(e["physical_gbs"] - (33569796 + 80000) / 14950) < 1e-6
+
+
+def test_record_traffic_needs_a_launch(tmp_path):
+    p = tmp_path / "t.csv"
+    p.write_text(CSV.splitlines()[0] + "\n" + CSV.splitlines()[1] + "\n")
     with pytest.raises(ValueError):
         bench.record_traffic(str(p), "w", "kda_bt16_kernel", "")
 

@@ -62,3 +62,28 @@ def test_far_block_is_invisible_on_kda_inputs_alone():
     good = ref.astype(np.float32).astype(np.float64)
     assert np.abs(ref.reshape(-1, 2, 64)[48:64, :, :16]).max() < 1e-6
     assert _verdict(inp, _zero_block(inp, good, 3, 0), ref)
+
+
+@pytest.mark.parametrize("layout", ["dense", "packed"])
+def test_parts_cover_the_input_and_agree_with_the_whole(layout):
+    """The part-by-part comparison of the large workloads sees every chunk exactly
+    once, and the oracle run on the parts equals the oracle run on the whole."""
+    if layout == "dense":
+        wl = ki.Workload("p", "dense", H=3, in_dtype="f32", out_dtype="f32", seed=4, B=5, T=130, kind="gauss")
+    else:
+        wl = ki.Workload("p", "packed", H=3, in_dtype="bf16", out_dtype="f32", seed=4,
+                         seqlens=(1, 200, 0, 64, 65, 7, 300), kind="gauss")
+    inp = ki.build(wl)
+    orc = oracle.get()
+    whole = orc.solve_tril(oracle.to_f64(inp.A), inp.cu_seqlens.numpy() if inp.cu_seqlens is not None else None)
+    whole = whole.reshape(-1, inp.H, 64)
+    seen = []
+    nparts = 0
+    for r0, nrows, A_sub, cu_sub, sub in parity.parts(inp, limit=7):
+        nparts += 1
+        ref = orc.solve_tril(oracle.to_f64(A_sub), cu_sub.numpy() if cu_sub is not None else None)
+        assert np.array_equal(ref.reshape(-1, inp.H, 64), whole[r0:r0 + nrows])
+        seen += [(r0 + a, n) for (a, n) in sub]
+        ok, msg = parity.check_solution(whole[r0:r0 + nrows], ref.reshape(-1, inp.H, 64), sub, 64, inp.A.dtype, F32)
+        assert ok, msg
+    assert seen == inp.chunks() and nparts > 2

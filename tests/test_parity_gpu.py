@@ -364,34 +364,18 @@ def test_specified_workloads(kda, orc, name):
     check_large(orc, inp, outs["auto"], out_dtype, name)
 
 
-def check_large(orc, inp, got, out_dtype, name, full_limit=40000, samples=1024):
-    """Every element against the oracle up to `full_limit` chunk-heads; above it
-    (too large for an all-element fp64 reference) every output element's
-    structure on the device and the values of `samples` sampled chunk-heads."""
+def check_large(orc, inp, got, out_dtype, name, slab_limit=40000):
+    """Every output element against the oracle, run part by part (whole batch rows
+    or whole requests of at most `slab_limit` chunk-heads) so that the fp64
+    reference of a part fits in host memory; and residuals of sampled chunk-heads."""
     H, bt = inp.H, inp.bt
-    ntask = len(inp.chunks()) * H
-    if ntask <= full_limit:
-        ref = oracle_ref(orc, inp)
-        check_full(inp, got, ref, out_dtype, name)
-    else:
-        g = got.view(-1, H, bt)
-        chunks = inp.chunks()
-        i_in = torch.tensor(row_geometry(inp)[0], device=DEV)
-        j = torch.arange(bt, device=DEV)
-        upper = (j[None, :] > i_in[:, None])[:, None, :].expand_as(g)
-        diag = (j[None, :] == i_in[:, None])[:, None, :].expand_as(g)
-        assert torch.all(g[upper] == 0) and torch.all(g[diag] == 1)
-        rng = np.random.default_rng(99)
-        Av = inp.A.view(-1, H, bt)
-        gh = g.cpu()
-        for t in rng.choice(ntask, samples, replace=False):
-            row0, n = chunks[t // H]
-            h = t % H
-            M = oracle.to_f64(Av[row0:row0 + n, h, :])
-            X = orc.invert_chunk(M, n, bt)[:n, :]
-            ok, worst, where = parity.check_tile(oracle.to_f64(gh[row0:row0 + n, h, :]), X, n,
-                                                 inp.A.dtype, out_dtype)
-            assert ok, (name, row0, h, where, worst)
+    g = got.view(-1, H, bt)
+    for r0, nrows, A_sub, cu_sub, sub_chunks in parity.parts(inp, slab_limit):
+        ref = orc.solve_tril(oracle.to_f64(A_sub), cu_sub.numpy() if cu_sub is not None else None)
+        got_sub = g[r0:r0 + nrows].to(torch.float64).cpu().numpy()
+        ok, msg = parity.check_solution(got_sub, ref.reshape(-1, H, bt), sub_chunks, bt, inp.A.dtype, out_dtype)
+        assert ok, f"{name} rows {r0}..{r0 + nrows}: {msg}"
+        del ref, got_sub
     check_residuals(inp, got, out_dtype, limit=1024)
 
 
@@ -530,7 +514,7 @@ def test_small_chunks_specified_shapes(kda, orc, bt, name):
     inp = ki.build(wl)
     out_dtype = ki.torch_dtype(wl.out_dtype)
     out, _ = solve(kda, inp, out_dtype, "single")
-    check_large(orc, inp, out, out_dtype, f"{name} bt={bt}", full_limit=200000)
+    check_large(orc, inp, out, out_dtype, f"{name} bt={bt}", slab_limit=200000)
 
 
 # --------------------------------------- input guard bands and similarity

@@ -109,6 +109,47 @@ def test_kgb_large_decay_offset(kda, orc):
     check(y, run(kda, y), reference(orc, y), F32, "offset")
 
 
+def _block_spans(x):
+    """Per-channel fall of g over every 16-row block of every chunk (nats)."""
+    g = x.g.double().numpy().reshape(-1, x.H, x.K)
+    spans = []
+    for row0, n in x.chunks():
+        for r in range(0, n, 16):
+            e = min(r + 15, n - 1)
+            spans.append(g[row0 + r] - g[row0 + e])
+    return np.stack(spans)
+
+
+STEEP_CASES = {
+    "packed": dict(layout="packed", seqlens=(1, 17, 64, 100, 0, 130, 33)),
+    "dense": dict(layout="dense", B=2, T=130),
+}
+
+
+@pytest.mark.parametrize("in_dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", list(STEEP_CASES))
+def test_kgb_steep_decays(kda, orc, in_dtype, case):
+    """Decays that fall 3 to 20 nats per token, and cliffs of 100 nats: blocks fall
+    far past FP32's exponent range (a factorisation through one reference row
+    overflows there), while the terms of nearby rows stay large."""
+    wl = ki.Workload("steep", H=3, in_dtype=NAMES[in_dtype], out_dtype="f32", seed=23, kind="steep",
+                     **STEEP_CASES[case])
+    x = ki.build_kgb(wl)
+    spans = _block_spans(x)
+    assert spans.max() > 400 and np.mean(spans > 80) > 0.4        # the inputs do what they claim
+    out = run(kda, x)
+    assert torch.isfinite(out).all()
+    check(x, out, reference(orc, x), F32, f"steep {case} {in_dtype}")
+
+
+@pytest.mark.parametrize("out_dtype", DTYPES, ids=str)
+def test_kgb_steep_decays_full_size(kda, orc, out_dtype):
+    """The 16 x 512-token, 64-head shape with steep decays, every element."""
+    wl = ki.WORKLOADS["packed_16x512_h64_f32"].with_(kind="steep", out_dtype=NAMES[out_dtype], seed=29)
+    x = ki.build_kgb(wl)
+    check(x, run(kda, x, out_dtype), reference(orc, x), out_dtype, f"steep full size -> {out_dtype}")
+
+
 def test_kgb_residual(kda, orc):
     x = ki.build_kgb(ki.Workload("res", "packed", H=4, in_dtype="f32", out_dtype="f32", seed=31,
                                  seqlens=(64, 100, 33)))
@@ -173,3 +214,4 @@ def test_kgb_argument_errors(kda):
     with pytest.raises(kda.KdaError) as e:
         kda.solve_tril_kgb(k[..., :16].contiguous(), g[..., :16].contiguous(), b)
     assert e.value.status == 2
+

@@ -80,6 +80,6 @@ def test_two_calls_match_regular_entry_point(lib):
 
 def test_rejects_shapes_beyond_the_builtin_workspace(lib):
     # dense [1, 65536, 64, 64] needs 1024 * 64 * 4 KiB = 256 MiB of workspace
-    st = lib.kda_solve_tril_split_static(1 << 20, 1 << 30, None, 0, 1, 65536, 64, 0, 0, None)
+    st = lib.kda_solve_tril_split_static(1 << 40, 1 << 44, None, 0, 1, 65536, 64, 0, 0, None)
     assert st == 3                                     # KDA_ERR_WORKSPACE, before any CUDA call
     assert lib.kda_solve_tril_workspace_size(1, 65536, 64, 0) > (64 << 20)
