@@ -76,8 +76,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // A tensor [rows, H, 64] viewed as 3-D {64 columns, H heads, rows}, with boxes of
-// {16 (w+1) columns, 1 head, 16 rows} for w = 0 .. n-1.
-bool encode_maps(const void *base, int32_t dt, int32_t H, int64_t rows, CUtensorMap *maps, int n) {
+// {width[w] columns, 1 head, box_rows rows} for w = 0 .. n-1.
+bool encode_maps(const void *base, int32_t dt, int32_t H, int64_t rows, CUtensorMap *maps, const int *width, int n,
+                 int box_rows) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const CUtensorMapDataType ty = dt == KDA_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -88,7 +89,7 @@ bool encode_maps(const void *base, int32_t dt, int32_t H, int64_t rows, CUtensor
     const cuuint64_t strides[2] = {kda::BT * es, cuuint64_t(H) * kda::BT * es};
     const cuuint32_t estr[3] = {1, 1, 1};
     for (int w = 0; w < n; ++w) {
-        const cuuint32_t box[3] = {cuuint32_t(16 * (w + 1)), 1, 16};
+        const cuuint32_t box[3] = {cuuint32_t(width[w]), 1, cuuint32_t(box_rows)};
         CUresult r = fn(&maps[w], ty, 3, const_cast<void *>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -97,10 +98,11 @@ bool encode_maps(const void *base, int32_t dt, int32_t H, int64_t rows, CUtensor
     return true;
 }
 
-// Input boxes (A, widths 16..64) and output boxes (Ai, widths 16..48, used to
-// store the zero blocks above the diagonal of full chunks).
-bool make_maps(const void *A, int32_t in_dt, void *Ai, int32_t out_dt, int32_t H, int64_t rows, kda::Maps &maps) {
-    return encode_maps(A, in_dt, H, rows, maps.m, 4) && encode_maps(Ai, out_dt, H, rows, maps.o, 3);
+// Input boxes of A: 16 rows x 16, 32, 48, 64 columns (the split kernels' block
+// rows), then 32 rows x 32 and 64 columns (the single pass's two boxes).
+bool make_maps(const void *A, int32_t in_dt, void *, int32_t, int32_t H, int64_t rows, kda::Maps &maps) {
+    static const int w16[4] = {16, 32, 48, 64}, w32[2] = {32, 64};
+    return encode_maps(A, in_dt, H, rows, maps.m, w16, 4, 16) && encode_maps(A, in_dt, H, rows, maps.m + 4, w32, 2, 32);
 }
 
 // Encoded tensor maps of recent calls, keyed by everything they encode (base
@@ -135,6 +137,30 @@ bool cached_maps(const void *A, int32_t in_dt, void *Ai, int32_t out_dt, int32_t
     g_map_val[g_map_next] = maps;
     g_map_next = (g_map_next + 1) % kMapCache;
     if (g_map_n < kMapCache) ++g_map_n;
+    return true;
+}
+
+// k [rows, H, K] (input dtype) and g [rows, H, K] (FP32) viewed as 3-D {K
+// channels, H heads, rows}, boxes of 32 channels x 1 head x 64 rows.
+bool encode_kg_maps(const void *k, int32_t in_dt, const float *g, int32_t H, int32_t K, int64_t rows,
+                    kda::KgbMaps &maps) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint32_t box[3] = {32, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    for (int t = 0; t < 2; ++t) {
+        const int32_t dt = t == 0 ? in_dt : KDA_F32;
+        const CUtensorMapDataType ty = dt == KDA_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : dt == KDA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const cuuint64_t es = cuuint64_t(elt_size(dt));
+        const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(H), cuuint64_t(rows)};
+        const cuuint64_t strides[2] = {cuuint64_t(K) * es, cuuint64_t(H) * cuuint64_t(K) * es};
+        CUresult r = fn(t == 0 ? &maps.k : &maps.g, ty, 3, const_cast<void *>(t == 0 ? k : static_cast<const void *>(g)),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return false;
+    }
     return true;
 }
 
@@ -466,12 +492,16 @@ kda_status_t kda_solve_tril_kgb(const void *k, const float *g, const void *beta,
     p.cpr = static_cast<int32_t>((T + kda::BT - 1) / kda::BT);
     p.n_tasks = static_cast<int32_t>(max_chunks(B, T, num_seqs) * H);
     p.K = K;
+    p.err = info.err;
+    kda::KgbMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode_kg_maps(k, in_dtype, g, H, K, int64_t(rows), maps)) return KDA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (in_dtype) {
-        case KDA_F32: e = kda::launch_kgb_f32(out_dtype, p, device, info.num_sms, s); break;
-        case KDA_BF16: e = kda::launch_kgb_bf16(out_dtype, p, device, info.num_sms, s); break;
-        default: e = kda::launch_kgb_f16(out_dtype, p, device, info.num_sms, s); break;
+        case KDA_F32: e = kda::launch_kgb_f32(out_dtype, maps, p, device, info.num_sms, s); break;
+        case KDA_BF16: e = kda::launch_kgb_bf16(out_dtype, maps, p, device, info.num_sms, s); break;
+        default: e = kda::launch_kgb_f16(out_dtype, maps, p, device, info.num_sms, s); break;
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

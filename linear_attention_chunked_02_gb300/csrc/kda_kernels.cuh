@@ -12,9 +12,12 @@
 //     (q = chunk * H + head, so neighbouring CTAs share the chunk's token rows).
 //   * Thread 0 issues TMA tile loads (cp.async.bulk.tensor, mbarrier
 //     completion) into a 2-stage ring, so the next chunk-head is in flight
-//     while the current one is computed.  Only the ten lower 16x16 blocks are
-//     fetched: block-row r as one box of 16 rows x 16(r+1) columns.  FP32 input
-//     is used in place from the landing buffer; 16-bit input is widened once.
+//     while the current one is computed.  The single pass fetches two boxes,
+//     rows 0-31 x columns 0-31 and rows 32-63 x columns 0-63: exactly the
+//     128-byte lines that hold the strictly lower triangle, in two TMA
+//     instructions (issuing a TMA instruction holds up thread 0's warp, so
+//     fewer, larger boxes shorten the critical path).  FP32 input is used in
+//     place from the landing buffer; 16-bit input is widened once.
 //   * Diagonal blocks: one unit per block, one lane per column, forward
 //     substitution in registers (FP32 FMA).
 //   * Merge, as two 32x32 levels (the 64x64 matrix is lower block-triangular
@@ -28,8 +31,7 @@
 //     straight from the landing buffer, and each intermediate T stays in
 //     registers as the next product's left operand.  One barrier per chunk-head.
 //   * Every output block is stored from the registers that computed it; the
-//     zero blocks above the diagonal of full chunks are TMA tensor stores from
-//     a zeroed shared-memory buffer.
+//     zero blocks above the diagonal are 16-byte vector stores.
 //   * Split path: MODE_DIAG inverts the diagonal blocks, writes them (and the
 //     zero blocks) to the output and their transposed FP32 tiles to the
 //     workspace; MODE_MERGE loads the tiles back and produces the
@@ -49,6 +51,10 @@ constexpr int BT = 64;          // chunk length
 constexpr int BS = 16;          // diagonal block size
 constexpr int NTHREADS = 64;    // four 16-lane units
 constexpr int STAGES = 2;
+
+// cu_seqlens entries cached in shared memory (packed batches of up to 255
+// requests); larger batches walk cu_seqlens in global memory
+constexpr int CU_CAP = 256;
 
 constexpr int MODE_FUSED = 0;
 constexpr int MODE_DIAG = 1;
@@ -155,21 +161,10 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
-// TMA tile store from shared memory (bulk async-group completion).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-        : "memory");
+// Prefetch a tensor map (kernel parameter) into the TMA descriptor cache.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until at most N committed bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Wait until every committed bulk group has completed (writes included).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // --------------------------------------------------------- dtype helpers
 template <typename T> struct Elt;
@@ -234,8 +229,9 @@ template <int MODE, typename TIn>
 struct Layout {
     static constexpr int ELT = sizeof(TIn);
     static constexpr bool WIDEN = ELT == 2;
-    // stage: raw TMA landing area
-    static constexpr int A_ELEMS = MODE == MODE_FUSED ? 10 * 256 : MODE == MODE_DIAG ? 4 * 256 : 6 * 256;
+    // stage: raw TMA landing area (single pass: rows 0-31 x 32 columns, then
+    // rows 32-63 x 64 columns; split kernels: 16-row boxes per block-row)
+    static constexpr int A_ELEMS = MODE == MODE_FUSED ? 32 * 32 + 32 * 64 : MODE == MODE_DIAG ? 4 * 256 : 6 * 256;
     static constexpr int A_BYTES = A_ELEMS * ELT;
     static constexpr int WS_OFF = (A_BYTES + 127) / 128 * 128;
     static constexpr int STAGE_BYTES = MODE == MODE_MERGE ? WS_OFF + 4096 : WS_OFF;
@@ -248,21 +244,20 @@ struct Layout {
     static constexpr int OFF_AF = OFF_STAGE + STAGES * STAGE_BYTES;
     static constexpr int OFF_XT = OFF_AF + NAF * ABS * 4;
     static constexpr int OFF_XR = OFF_XT + (MODE == MODE_DIAG ? 0 : 4 * XTS * 4);
-    // 16 x 48 zero elements (FP32-sized) that TMA stores copy into the blocks
-    // above the diagonal of full chunks
-    static constexpr int Z_BYTES = MODE == MODE_MERGE ? 0 : 16 * 48 * 4;
-    static constexpr int OFF_Z = OFF_XT + X_BYTES;
-    static constexpr int BYTES = OFF_Z + Z_BYTES;
-    static_assert(OFF_Z % 128 == 0 && OFF_STAGE % 128 == 0 && STAGE_BYTES % 128 == 0,
-                  "TMA source/destination buffers must be 128-byte aligned");
-    // stage offset (bytes) of block-row r's box, and the box width in elements
+    // cu_seqlens of a packed batch of up to CU_CAP - 1 requests, so that the
+    // per-task walk reads shared rather than global memory
+    static constexpr int OFF_CU = OFF_XT + X_BYTES;
+    static constexpr int BYTES = OFF_CU + CU_CAP * 4;
+    static_assert(OFF_STAGE % 128 == 0 && STAGE_BYTES % 128 == 0,
+                  "TMA destination buffers must be 128-byte aligned");
+    // stage offset (bytes) of block-row r's first row, and its row pitch in elements
     __host__ __device__ static constexpr int row_off(int r) {
-        return MODE == MODE_FUSED ? 256 * ELT * (r * (r + 1) / 2)
+        return MODE == MODE_FUSED ? (r < 2 ? 16 * 32 * ELT * r : 32 * 32 * ELT + 16 * 64 * ELT * (r - 2))
              : MODE == MODE_DIAG  ? 256 * ELT * r
                                   : 256 * ELT * ((r - 1) * r / 2);
     }
     __host__ __device__ static constexpr int width(int r) {
-        return MODE == MODE_FUSED ? 16 * (r + 1) : MODE == MODE_DIAG ? 16 : 16 * r;
+        return MODE == MODE_FUSED ? (r < 2 ? 32 : 64) : MODE == MODE_DIAG ? 16 : 16 * r;
     }
     static constexpr int R0 = MODE == MODE_MERGE ? 1 : 0;   // first block-row fetched
 };
@@ -322,9 +317,10 @@ __device__ __forceinline__ Meta locate(const P &p, int32_t c, int32_t h, Walk &w
         m.valid = 1;
         return m;
     }
-    // advance to the request that holds chunk c
+    // advance to the request that holds chunk c (p.cu may point to global or
+    // shared memory: generic loads)
     while (w.s < p.nseq) {
-        const int32_t a = __ldg(p.cu + w.s), b = __ldg(p.cu + w.s + 1);
+        const int32_t a = p.cu[w.s], b = p.cu[w.s + 1];
         const int32_t nc = nchunks<CBT>(a, b);
         if (c < w.cbase + nc) {
             int64_t r0 = int64_t(a) + int64_t(c - w.cbase) * CBT;
@@ -344,23 +340,43 @@ __device__ __forceinline__ Meta locate(const P &p, int32_t c, int32_t h, Walk &w
     return m;
 }
 
-// Chunk-head q -> (first row, valid rows, head) for chunk length CBT; P has the
-// layout fields cu, nseq, H, T, cpr, n_tasks.  Tasks of one walker increase.
-template <int CBT = BT, typename P>
-__device__ __forceinline__ Meta decode(const P &p, int32_t q, Walk &w) {
-    if (q >= p.n_tasks) return Meta{0, 0, 0, 0};
-    const int32_t c = q / p.H;
-    return locate<CBT>(p, c, q - c * p.H, w);
-}
+// Chunk-heads q = q0, q0 + step, ... of one walker: chunk c = q / H and head
+// h = q % H advanced incrementally (two divisions at the start only).
+struct TaskWalk {
+    int32_t q, c, h, step, sc, sh;
+    Walk w;
+    template <typename P>
+    __device__ __forceinline__ TaskWalk(const P &p, int32_t q0, int32_t step_) : q(q0), step(step_), w{0, 0} {
+        c = q0 / p.H;
+        h = q0 - c * p.H;
+        sc = step_ / p.H;
+        sh = step_ - sc * p.H;
+    }
+    // meta of the current chunk-head (q returned in *qout), then advance
+    template <int CBT = BT, typename P>
+    __device__ __forceinline__ Meta next(const P &p, int32_t *qout = nullptr) {
+        const Meta m = q < p.n_tasks ? locate<CBT>(p, c, h, w) : Meta{0, 0, 0, 0};
+        if (qout != nullptr) *qout = q;
+        q += step;
+        c += sc;
+        h += sh;
+        if (h >= p.H) {
+            h -= p.H;
+            ++c;
+        }
+        return m;
+    }
+};
 
-// Issue the loads of task q into stage `st` (one thread).
+// Issue the loads of the walker's next task into stage `st` (one thread).
 template <int MODE, typename TIn>
-__device__ __forceinline__ void issue(const Params &p, const CUtensorMap *maps, int32_t q, Walk &w,
+__device__ __forceinline__ void issue(const Params &p, const CUtensorMap *maps, TaskWalk &walk,
                                       unsigned char *smem, int st) {
     using L = Layout<MODE, TIn>;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR) + st;
     Meta *meta = reinterpret_cast<Meta *>(smem + L::OFF_META) + st;
-    const Meta m = decode(p, q, w);
+    int32_t q;
+    const Meta m = walk.next(p, &q);
     *meta = m;
     if (!m.valid) {
         mbar_arrive(bar);
@@ -368,10 +384,9 @@ __device__ __forceinline__ void issue(const Params &p, const CUtensorMap *maps, 
     }
     unsigned char *stage = smem + L::OFF_STAGE + st * L::STAGE_BYTES;
     mbar_arrive_expect_tx(bar, L::TX_BYTES);
-    if (MODE == MODE_FUSED) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            tma_load_3d(stage + L::row_off(r), &maps[r], 0, m.h, m.row0 + 16 * r, bar);
+    if (MODE == MODE_FUSED) {                // maps[4]: 32 x 32 box, maps[5]: 64 x 32 box
+        tma_load_3d(stage, &maps[4], 0, m.h, m.row0, bar);
+        tma_load_3d(stage + L::row_off(2), &maps[5], 0, m.h, m.row0 + 32, bar);
     } else if (MODE == MODE_DIAG) {
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -633,8 +648,8 @@ __device__ __forceinline__ void store_upper_zeros(TOut *ob, int os, int n, int t
 
 // ----------------------------------------------------------------- kernel
 struct Maps {
-    CUtensorMap m[4];          // A: box widths 16, 32, 48, 64 columns; 16 rows; 1 head
-    CUtensorMap o[3];          // Ai: box widths 16, 32, 48 columns; 16 rows; 1 head
+    CUtensorMap m[6];          // A: box widths 16, 32, 48, 64 columns x 16 rows (split kernels),
+                               // then 32 and 64 columns x 32 rows (single pass); 1 head
 };
 
 template <int MODE, typename TIn, typename TOut>
@@ -651,23 +666,32 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     TOut *out = reinterpret_cast<TOut *>(p.out);
     const int tid = threadIdx.x;
     const int unit = tid >> 4, warp = tid >> 5;
+    // the task walk reads cu_seqlens from shared memory when it fits
+    Params ps = p;
+    if (p.cu != nullptr && p.nseq < CU_CAP) {
+        int32_t *cs = reinterpret_cast<int32_t *>(smem + L::OFF_CU);
+        for (int i = tid; i <= p.nseq; i += NTHREADS) cs[i] = __ldg(p.cu + i);
+        ps.cu = cs;
+        __syncthreads();
+    }
     const int l = tid & 15;                  // lane in the 16-lane unit (diagonal inverse)
     const int lane = tid & 31, g = lane >> 2, t = lane & 3;   // mma fragment coordinates
     const int32_t G = gridDim.x;
     const int os = p.H * BT;                 // output row stride (elements)
-    Walk walk{0, 0};
+    TaskWalk walk(p, int32_t(blockIdx.x), G);   // thread 0's walk over the tasks it loads
 
-    if (MODE != MODE_MERGE) {                // zero source of the TMA stores
-        float4 *z = reinterpret_cast<float4 *>(smem + L::OFF_Z);
-        for (int i = tid; i < L::Z_BYTES / 16; i += NTHREADS) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     if (tid == 0) {
+        // the tensor maps this kernel uses, into the TMA unit's descriptor cache
+        if (MODE == MODE_FUSED) {
+            prefetch_tensormap(&maps.m[4]);
+            prefetch_tensormap(&maps.m[5]);
+        } else {
+            for (int r = 0; r < 4; ++r) prefetch_tensormap(&maps.m[r]);
+        }
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
-        for (int s = 0; s < STAGES; ++s)
-            issue<MODE, TIn>(p, maps.m, int32_t(blockIdx.x) + s * G, walk, smem, s);
+        for (int s = 0; s < STAGES; ++s) issue<MODE, TIn>(ps, maps.m, walk, smem, s);
     }
-    fence_proxy_async();                     // zero buffer visible to the TMA engine
     __syncthreads();
 
     for (int it = 0;; ++it) {
@@ -682,7 +706,6 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
                 mbar_wait_bounded(&bars[st], parity);
                 for (int s = 1; s < STAGES; ++s)
                     mbar_wait_bounded(&bars[(st + s) % STAGES], ((it + s) / STAGES) & 1);
-                bulk_wait_all();
             }
             return;
         }
@@ -695,23 +718,11 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         // iterations ahead (the prologue issued iterations 0 .. STAGES - 1).
         if (it >= 1 && tid == 0) {
             fence_proxy_async();
-            issue<MODE, TIn>(p, maps.m, q + (STAGES - 1) * G, walk, smem, (it + STAGES - 1) % STAGES);
+            issue<MODE, TIn>(ps, maps.m, walk, smem, (it + STAGES - 1) % STAGES);
         }
         TOut *ob = out + (int64_t(m.row0) * p.H + m.h) * BT;      // chunk-head's first row
 
-        if (MODE != MODE_MERGE) {            // zero blocks above the diagonal
-            if (m.n == BT) {
-                if (tid == 0) {
-#pragma unroll
-                    for (int br = 0; br < 3; ++br)
-                        tma_store_3d(&maps.o[2 - br], smem + L::OFF_Z, 16 * (br + 1), m.h, m.row0 + 16 * br);
-                    bulk_commit();
-                    bulk_wait_read<2>();
-                }
-            } else {
-                store_upper_zeros(ob, os, m.n, tid);
-            }
-        }
+        if (MODE != MODE_MERGE) store_upper_zeros(ob, os, m.n, tid);   // zero blocks above the diagonal
 
         // A operands: the landing buffer itself (rows past a partial chunk's end
         // zeroed), plus FP32 copies of the diagonal blocks for 16-bit input
@@ -835,7 +846,24 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             out_tile_t(ob, os, m.n, 3, warp, cx, g, t);
         }
     }
-    if (MODE != MODE_MERGE && tid == 0) bulk_wait_all();      // zero-block stores complete
 }
+
+// ------------------------------------------------------- named barriers
+// Named barriers of 64 threads (one pair of warps) with the barrier id in a
+// register, so that every pair runs the same code (one copy of the solve in
+// the instruction cache, whatever the number of pairs).
+__device__ __forceinline__ bool bar64_and(int id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, 64, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(v)), "r"(id)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void bar64(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
 }  // namespace kda

@@ -1,50 +1,62 @@
-// kda_kgb.cuh -- KDA's chunk matrix built from keys, betas and decays, fused
-// with the 64-token solve: A never leaves shared memory.
+// kda_kgb.cuh -- KDA's chunk matrix built from keys, betas and decays on the
+// fifth-generation tensor cores (tcgen05, accumulator in tensor memory), fused
+// with the 64-token solve: A never leaves the SM.
 //
 // LightLLM PR #1703 (PR description) has KDA prefill use the shared solver;
 // the matrix it inverts is KDA's intra-chunk matrix
 //     A[i][j] = beta_i sum_d k_id k_jd exp(g_id - g_jd),   j < i,
-// with g the per-channel cumulative log decay.  Per chunk-head this kernel
-// builds the ten lower 16x16 blocks of A and solves (I + A)^-1 with the
-// 64-token kernel's schedule.
+// with g the per-channel cumulative log decay (non-increasing along a chunk).
 //
-// Construction.  Block I of the chunk has first row rI = 16 I and last live
-// row eI = min(16 I + 15, n - 1).  For block (I, J), I >= J:
-//     A_IJ = (Q_I * f_IJ) P_J^T,  Q_I[i][d] = k_id exp(g_id - g_rI,d),
-//     P_J[j][d] = k_jd exp(g_eJ,d - g_jd),  f_IJ[d] = exp(g_rI,d - g_eJ,d).
-// g is non-increasing along the chunk (a cumulative log decay), so every
-// exponent of Q and P is <= 0, and so is f's for I > J: none of these factors
-// can overflow, and one that underflows stands for a term below FP32's range.
-// Only the diagonal factor f_II = exp(span) with span = g_rI - g_eI >= 0
-// grows: channels whose span exceeds KGB_SAFE_SPAN get f_II = 0, and their
-// terms k_id k_jd exp(g_id - g_jd) are added to the diagonal block one by one
-// (a slow path that KDA's ordinary decays, about 1 nat per token, never take).
-// The products run on the tensor cores in split TF32 (mma.sync m16n8k8, hi/lo
-// parts, FP32 accumulation).
+// Construction.  With one reference value c_d per channel (g of the chunk's
+// middle live row),
+//     A = beta * strict_lower(Q P^T),  Q[i][d] = k_id 2^{(g_id - c_d) log2 e},
+//                                      P[j][d] = k_jd 2^{(c_d - g_jd) log2 e},
+// one 64 x 64 x K product per chunk-head.  A channel whose decay over the
+// chunk's live rows takes g further than KGB_TC_SAFE nats from c_d on either
+// side would lose accuracy in these factors (the rounding of the exponent grows
+// with its size) or overflow them: it is left out of the product (Q = P = 0)
+// and its terms k_id k_jd exp(g_id - g_jd) are added one by one (a slow path
+// that KDA's ordinary decays, about one nat per token, never take).
 //
-// Work split (one persistent CTA of 128 threads per resident slot, one
-// chunk-head at a time):
-//   * warp w streams channels 32w .. 32w+31 of the chunk's k and g rows into
-//     shared memory with cp.async and turns them into Q and P in place (one
-//     lane per channel; rows past a partial chunk's end become zeros);
-//   * each warp computes two or three of the ten blocks over all channels
-//     and writes them, times beta and masked to the strict lower part of the
-//     chunk's valid rows, into an FP32 A tile;
-//   * warps 0 and 1 solve the tile exactly like the 64-token kernel (diagonal
-//     forward substitution, two merge levels on the tensor cores) while the
-//     next chunk-head's rows are in flight and warps 2 and 3 start on them.
+// FP32 accuracy on TF32 tensor cores: Q = Qh + Ql and P = Ph + Pl with Qh, Ph
+// truncated to TF32 and Ql, Pl the TF32 remainders.  The A operand of one
+// tcgen05.mma (M = 128) stacks [Qh; Ql], the B operand (N = 128) stacks
+// [Ph; Pl]; the FP32 accumulator D (128 TMEM lanes x 128 columns) then holds
+// Qh Ph^T, Qh Pl^T (rows 0-63) and Ql Ph^T (rows 64-127, columns 0-63), whose
+// sum is Q P^T to about 2^-22 relative (the dropped Ql Pl^T is the fourth
+// quadrant).  K = 128 channels take 16 instructions of K = 8.
+//
+// One persistent CTA per SM, 16 warps in four roles; every role walks the
+// chunk-heads q = blockIdx.x + c * gridDim.x in the same order:
+//   * warp 0, lane 0 (loader): TMA loads of each chunk-head's k and g, one
+//     slice of 32 channels at a time, into a ring of KGB_NST staging slots;
+//   * warp 1, lane 0 (MMA issue): for every slice whose operands are ready,
+//     four tcgen05.mma of K = 8 into TMEM buffer c % 2, with tcgen05.commit
+//     releasing the operand buffer and, after a chunk-head's last slice, the
+//     accumulator.  Issuing a TMA or tensor-core instruction holds the issuing
+//     warp for a while, so the two streams run on warps of their own;
+//   * warps 2-7 (transform): each slice of the staging ring into the four TF32
+//     operand parts in a 128-byte-swizzled buffer (two-slice ring); every warp
+//     signals the MMA warp on its own mbarrier arrival, without a group barrier;
+//   * warps 8-11 (epilogue): tcgen05.ld of the accumulator rows (warp w reads
+//     TMEM lanes 32 (w % 4) .. + 31), the three quadrants added, beta and the
+//     strict-lower and live-row masks applied, any steep channels' terms added,
+//     into the ten lower 16 x 16 blocks of the A tile of solve pair c % 2;
+//   * warps 12-13 and 14-15 (solve pairs 0, 1): the 64-token solve of the A
+//     tile (diagonal forward substitution, two merge levels on mma.sync) for
+//     the chunk-heads c with c % 2 == pair.  The pairs share one copy of the
+//     solve's code (barrier ids in registers).
+// Hand-offs are mbarriers with bounded waits: staging slot full (TMA bytes) and
+// empty (transform warps), operand buffer full (transform warps) and empty (MMA
+// commit), accumulator full (MMA commit + the producer's release arrive) and
+// empty (epilogue), A tile full (epilogue) and empty (solve pair).
 #pragma once
 
 #include "kda_kernels.cuh"
 #include "kda_small.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
-
-// factor rows per slice: the six block pairs I > J, then the four diagonal blocks
-constexpr int KGB_FROWS = 10;
-// largest decay (nats) over a diagonal block that its tensor-core product takes,
-// in log2 units; steeper channels go through the slow path
-constexpr float KGB_SAFE_SPAN2 = 32.0f * 1.4426950408889634f;
 
 struct KgbParams {
     const void *k;             // [rows, H, K], input dtype
@@ -58,24 +70,63 @@ struct KgbParams {
     int32_t cpr;               // dense: chunks per batch row
     int32_t n_tasks;           // loop bound on chunk-head indices
     int32_t K;                 // channels: 32, 64, 96 or 128
+    unsigned *err;             // device error word
 };
 
-constexpr int KGB_THREADS = 128;
-// slice row pitch (floats): the paired 8-byte fragment loads at 8 g + 2 t hit 32
-// distinct banks per half-warp
-constexpr int KGB_SP = 40;
-constexpr int KGB_SLICE = 64 * KGB_SP;         // floats per slice buffer
-constexpr int KGB_FLOATS = 2 * 4 * KGB_SLICE   // Q and P slices
-                         + 4 * KGB_FROWS * 32  // f_IJ per slice, block pair and diagonal block
-                         + 10 * 256            // A blocks, pitch 16
-                         + 4 * XTS + 4 * XRS   // inverse tiles of the merge
-                         + 64                  // beta of the chunk's rows
-                         + 16;                 // steep-channel masks [slice][diagonal block]
-constexpr int KGB_BYTES = KGB_FLOATS * 4;
+// Tensor maps of k and g viewed as {K channels, H heads, rows}, boxes of 32
+// channels x 1 head x 64 rows.
+struct KgbMaps {
+    CUtensorMap k, g;
+};
 
-__device__ __forceinline__ void named_sync64() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+constexpr int KGB_THREADS = 512;
+constexpr int KGB_TWARPS = 6;                      // transform warps 2 .. 7
+constexpr int KGB_EW0 = 2 + KGB_TWARPS;            // first of the four epilogue warps
+constexpr int KGB_SW0 = KGB_EW0 + 4;               // first solve warp
+constexpr int KGB_PAIRS = (KGB_THREADS / 32 - KGB_SW0) / 2;   // solve pairs
+constexpr int KGB_TTHREADS = 32 * KGB_TWARPS;
+// largest distance (nats) of g from the channel's reference over the chunk that
+// the tensor-core product takes; further channels go through the slow path
+constexpr float KGB_TC_SAFE = 48.0f;
 
-// Chunk-heads q = q0, q0 + step, ... of one CTA (every thread walks the same sequence).
+// staging ring of raw k and g slices (one 64-row x 32-channel box of each)
+constexpr int KGB_NST = 4;
+constexpr int KGB_STAGE_BYTES = 2 * 64 * 128;      // k box (<= 8 KiB), then the g box at +8 KiB
+constexpr int KGB_STAGE_G = 64 * 128;
+
+// mbarriers
+constexpr int BAR_ST_FULL = 0;                     // [KGB_NST]
+constexpr int BAR_ST_EMPTY = KGB_NST;              // [KGB_NST]
+constexpr int BAR_OPS_FULL = 2 * KGB_NST;          // [2]
+constexpr int BAR_OPS_EMPTY = BAR_OPS_FULL + 2;    // [2]
+constexpr int BAR_D_FULL = BAR_OPS_EMPTY + 2;      // [2]
+constexpr int BAR_D_EMPTY = BAR_D_FULL + 2;        // [2]
+constexpr int BAR_AT_FULL = BAR_D_EMPTY + 2;       // [KGB_PAIRS]
+constexpr int BAR_AT_EMPTY = BAR_AT_FULL + KGB_PAIRS;   // [KGB_PAIRS]
+constexpr int KGB_NBARS = BAR_AT_EMPTY + KGB_PAIRS;
+
+// shared memory (bytes)
+constexpr int KGB_OFF_BAR = 0;
+constexpr int KGB_OFF_TMEM = KGB_NBARS * 8;        // TMEM base address written by tcgen05.alloc
+// steep-channel masks [8 chunk-heads][4 slices]: a ring deep enough that the
+// transform cannot overwrite a chunk-head's masks before its epilogue is done
+constexpr int KGB_OFF_STEEP = KGB_OFF_TMEM + 64;
+constexpr int KGB_OFF_OPS = 1024;                  // [2 slices] {A: 128 x 128 B, B: 128 x 128 B}
+constexpr int KGB_OPS_BYTES = 2 * 128 * 128;
+constexpr int KGB_OFF_STAGE = KGB_OFF_OPS + 2 * KGB_OPS_BYTES;   // [KGB_NST] staging slots
+constexpr int KGB_OFF_AT = KGB_OFF_STAGE + KGB_NST * KGB_STAGE_BYTES;  // [pairs] A tile, 10 blocks of 16 x 16
+constexpr int KGB_OFF_X = KGB_OFF_AT + KGB_PAIRS * 10 * 256 * 4;       // [pairs] inverse tiles of the merge
+constexpr int KGB_X_FLOATS = 4 * XTS + 4 * XRS;
+constexpr int KGB_OFF_SC = KGB_OFF_X + KGB_PAIRS * KGB_X_FLOATS * 4;   // slow path: one channel's k and g, 64 rows
+constexpr int KGB_BYTES = KGB_OFF_SC + 2 * 64 * 4 + 1024;      // + alignment slack
+static_assert(KGB_OFF_STEEP + 8 * 4 * 4 <= KGB_OFF_OPS, "header fits");
+static_assert(KGB_OFF_OPS % 1024 == 0 && KGB_OPS_BYTES % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+static_assert(KGB_OFF_STAGE % 128 == 0 && KGB_STAGE_BYTES % 128 == 0, "TMA destinations are 128-byte aligned");
+
+constexpr uint32_t KGB_TMEM_COLS = 512;            // the whole TMEM of the SM (one CTA per SM)
+constexpr uint32_t KGB_IDESC = tc::idesc_tf32<128, 128>();
+
+// Chunk-heads q = q0, q0 + step, ... (every thread of a group walks the same sequence).
 struct KgbWalk {
     int32_t q, c, h, step, sc, sh;
     Walk w;
@@ -99,34 +150,6 @@ struct KgbWalk {
     }
 };
 
-// Channels 32 s .. 32 s + 31 of the chunk-head's k and g rows into the slice
-// buffers (row pitch KGB_SP floats; 16-bit keys land at the start of each row).
-template <typename TIn>
-__device__ __forceinline__ void kgb_issue(const KgbParams &p, const Meta &m, int s, float *kb, float *gb, int lane) {
-    if (!m.valid) return;
-    constexpr int VEC = Elt<TIn>::VEC;
-    constexpr int CK = 32 / VEC;                       // 16-byte copies per key row
-    const int64_t rs = int64_t(p.H) * p.K;             // row stride (elements)
-    const int64_t base = int64_t(m.row0) * rs + int64_t(m.h) * p.K + 32 * s;
-    const TIn *ks = reinterpret_cast<const TIn *>(p.k) + base;
-    const float *gs = p.g + base;
-#pragma unroll 4
-    for (int e = lane; e < 64 * CK; e += 32) {
-        const int i = e / CK, c = e % CK;
-        const bool live = i < m.n;
-        cp_async16(reinterpret_cast<unsigned char *>(kb + i * KGB_SP) + 16 * c, live ? ks + i * rs + c * VEC : p.k,
-                   live ? 16u : 0u);
-    }
-#pragma unroll 4
-    for (int e = lane; e < 64 * 8; e += 32) {
-        const int i = e >> 3, c = e & 7;
-        const bool live = i < m.n;
-        cp_async16(gb + i * KGB_SP + 4 * c, live ? gs + i * rs + 4 * c : p.g, live ? 16u : 0u);
-    }
-}
-
-// Lane d of the slice's warp: the block-pair factors of channel d, then Q and
-// P of channel d in place (column d of the slice is touched by this lane only).
 // 2^x on the SFU (PTX ex2.approx.ftz.f32; relative error about 2^-22)
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -134,169 +157,130 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-template <typename TIn>
-__device__ __forceinline__ void kgb_transform(float *kb, float *gb, float *fac, unsigned *steep, int n, int d) {
-    // exponents are differences of g taken first (exact for nearby values), then
-    // scaled to base 2, so their error does not grow with |g|
-    constexpr float LOG2E = 1.4426950408889634f;
-    float gr[4], ge[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int e = 16 * b + 15 < n ? 16 * b + 15 : n - 1;
-        gr[b] = gb[16 * b * KGB_SP + d];
-        ge[b] = gb[(e > 0 ? e : 0) * KGB_SP + d];
-    }
-    // f_IJ = exp(g_rI - g_eJ), I > J (zero when block I starts past the chunk's end)
-#pragma unroll
-    for (int I = 1; I < 4; ++I)
-#pragma unroll
-        for (int J = 0; J < I; ++J)
-            fac[(I * (I - 1) / 2 + J) * 32 + d] = 16 * I < n ? ex2((gr[I] - ge[J]) * LOG2E) : 0.f;
-    // f_II = exp(g_rI - g_eI), zero for a channel that falls further than the
-    // safe span over the block (its terms take the slow path)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const float span = (gr[b] - ge[b]) * LOG2E;
-        const bool live = 16 * b < n, st = live && !(span <= KGB_SAFE_SPAN2);
-        fac[(6 + b) * 32 + d] = live && !st ? ex2(span) : 0.f;
-        const unsigned m = __ballot_sync(0xffffffffu, st);
-        if (d == 0) steep[b] = m;
-    }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        float kv[16];
-        if constexpr (sizeof(TIn) == 4) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) kv[i] = kb[(16 * b + i) * KGB_SP + d];
-        } else {                                       // raw 16-bit keys at the start of each row
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                kv[i] = float(reinterpret_cast<const TIn *>(kb + (16 * b + i) * KGB_SP)[d]);
-            }
-            __syncwarp();                              // every lane has read the raw row before it is widened
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = 16 * b + i;
-            const bool live = r < n;
-            const float gv = gb[r * KGB_SP + d];
-            kb[r * KGB_SP + d] = live ? kv[i] * ex2((gv - gr[b]) * LOG2E) : 0.f;    // Q
-            gb[r * KGB_SP + d] = live ? kv[i] * ex2((ge[b] - gv) * LOG2E) : 0.f;    // P
-        }
-    }
+template <int ID, int N>
+__device__ __forceinline__ void named_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
+// Named barrier that also ANDs a flag over its N threads (so that a group
+// leaves its loop together, never stranding a member at a later barrier).
+template <int ID, int N>
+__device__ __forceinline__ bool named_sync_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(v)), "n"(ID), "n"(N)
+        : "memory");
+    return r != 0;
 }
 
-// Slow path of diagonal block I: the terms of the channels in the steep masks,
-// k_id k_jd exp(g_id - g_jd) one by one, read again from global memory, added to
-// the lane's C fragments (rows g, g + 8; columns 8 nt + 2 t + e).
-template <typename TIn>
-__device__ __forceinline__ void kgb_steep_terms(const KgbParams &p, const Meta &m, const unsigned *steep, int I,
-                                             int nsl, int g, int t, TileC &c) {
-    constexpr float LOG2E = 1.4426950408889634f;
-    const int64_t rs = int64_t(p.H) * p.K;
-    const int64_t base = (int64_t(m.row0) + 16 * I) * rs + int64_t(m.h) * p.K;
-    const TIn *kp = reinterpret_cast<const TIn *>(p.k) + base;
-    const float *gp = p.g + base;
-    const int li[2] = {g, g + 8};
-    const int lj[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-    for (int s = 0; s < nsl; ++s) {
-        unsigned mask = steep[s * 4 + I];
-        while (mask != 0u) {
-            const int d = 32 * s + __ffs(mask) - 1;
-            mask &= mask - 1u;
-            float ki[2], gi[2], kj[4], gj[4];
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-                const bool live = 16 * I + li[a] < m.n;
-                ki[a] = live ? float(kp[li[a] * rs + d]) : 0.f;
-                gi[a] = live ? gp[li[a] * rs + d] : 0.f;
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const bool live = 16 * I + lj[a] < m.n;
-                kj[a] = live ? float(kp[lj[a] * rs + d]) : 0.f;
-                gj[a] = live ? gp[lj[a] * rs + d] : 0.f;
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int a = 2 * nt + e;
-                        if (lj[a] < li[h])      // strictly lower; dead rows hold k = 0
-                            c.c[nt][2 * h + e] = fmaf(ki[h] * kj[a], ex2((gi[h] - gj[a]) * LOG2E), c.c[nt][2 * h + e]);
-                    }
-        }
-    }
+// Wait for phase `parity` of an mbarrier; false (and the error word set) after
+// WAIT_LIMIT_NS.
+__device__ __forceinline__ bool kgb_wait(uint64_t *bars, int b, uint32_t parity, unsigned *err) {
+    if (mbar_wait_bounded(&bars[b], parity)) return true;
+    atomicOr(err, ERR_WAIT_TIMEOUT);
+    return false;
 }
 
-// Block (I, J) of A over all nsl slices, times beta, masked, into Ab (pitch 16).
+// --------------------------------------------------------- transform group
+// TMA loads of slice s (channels 32 s .. 32 s + 31) of chunk-head m's 64 rows
+// of k and g into a staging slot (rows past the tensor's end are zero-filled;
+// rows past the chunk's end are masked by the transform).
 template <typename TIn>
-__device__ __forceinline__ void kgb_block(const KgbParams &p, const Meta &m, const float *kq, const float *gp,
-                                          const float *fac, const unsigned *steep, const float *bs, float *Ab,
-                                          int I, int J, int nsl, int g, int t) {
-    const int n = m.n;
-    TileC c;
-    zero(c);
-    const int pr = I > J ? I * (I - 1) / 2 + J : 6 + I;
-    for (int s = 0; s < nsl; ++s) {
-        const float *q0 = kq + s * KGB_SLICE + (16 * I + g) * KGB_SP;
-        const float *q1 = q0 + 8 * KGB_SP;
-        const float *pb = gp + s * KGB_SLICE + (16 * J + g) * KGB_SP;
-        const float *fs = fac + (s * KGB_FROWS + pr) * 32;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            // k-slots t and t + 4 of this k-step stand for channels 8 ks + 2t and 8 ks + 2t + 1
-            const int d0 = 8 * ks + 2 * t;
-            const float2 f = *reinterpret_cast<const float2 *>(fs + d0);
-            const float2 x0 = *reinterpret_cast<const float2 *>(q0 + d0);
-            const float2 x1 = *reinterpret_cast<const float2 *>(q1 + d0);
-            uint32_t ah[4], al[4];
-            split_tf32(x0.x * f.x, ah[0], al[0]);
-            split_tf32(x1.x * f.x, ah[1], al[1]);
-            split_tf32(x0.y * f.y, ah[2], al[2]);
-            split_tf32(x1.y * f.y, ah[3], al[3]);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float *pj = pb + 8 * nt * KGB_SP;
-                uint32_t bh0, bl0, bh1, bl1;
-                const float2 y = *reinterpret_cast<const float2 *>(pj + d0);
-                split_tf32(y.x, bh0, bl0);
-                split_tf32(y.y, bh1, bl1);
-                mma8(c.c[nt], al, bh0, bh1);
-                mma8(c.c[nt], ah, bl0, bl1);
-                mma8(c.c[nt], ah, bh0, bh1);
-            }
-        }
-    }
-    if (I == J) {
-        unsigned any = 0u;
-        for (int s = 0; s < nsl; ++s) any |= steep[s * 4 + I];
-        if (any != 0u) kgb_steep_terms<TIn>(p, m, steep, I, nsl, g, t, c);
-    }
-    // C fragments: c[nt][2 h + e] = block row g + 8 h, block column 8 nt + 2 t + e
-    float *Ad = Ab + blk(I, J) * 256;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int i = g + 8 * h, r = 16 * I + i, j = 8 * nt + 2 * t;
-            const float b = bs[r];
-            const bool live = r < n;
-            float v0 = c.c[nt][2 * h], v1 = c.c[nt][2 * h + 1];
-            if (I == J) {
-                v0 = j < i ? v0 : 0.f;
-                v1 = j + 1 < i ? v1 : 0.f;
-            }
-            *reinterpret_cast<float2 *>(Ad + i * 16 + j) = live ? make_float2(b * v0, b * v1) : make_float2(0.f, 0.f);
-        }
+__device__ __forceinline__ void kgb_tma_slice(const KgbMaps &maps, const Meta &m, int s, unsigned char *slot,
+                                              uint64_t *full) {
+    constexpr uint32_t BYTES = 64 * 32 * sizeof(TIn) + 64 * 32 * 4;
+    mbar_arrive_expect_tx(full, BYTES);
+    tma_load_3d(slot, &maps.k, 32 * s, m.h, m.row0, full);
+    tma_load_3d(slot + KGB_STAGE_G, &maps.g, 32 * s, m.h, m.row0, full);
 }
 
-// Solve of the A tile by threads 0..63 (the 64-token kernel's schedule on an
-// FP32 tile with blocks (i, j) at Ab + 256 blk(i, j), pitch 16).
+__device__ __forceinline__ void load4(const unsigned char *row, int c, const float *, float (&v)[4]) {
+    const float4 x = *reinterpret_cast<const float4 *>(row + 16 * c);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <typename T16>
+__device__ __forceinline__ void load4(const unsigned char *row, int c, const T16 *, float (&v)[4]) {
+    const uint2 x = *reinterpret_cast<const uint2 *>(row + 8 * c);
+    const T16 *h = reinterpret_cast<const T16 *>(&x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = float(h[i]);
+}
+
+__device__ __forceinline__ void split4(const float (&v)[4], uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) split_tf32(v[i], h[i], l[i]);
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Slice in the staging slot -> the four operand parts in the swizzled buffer
+// `ops` (A rows 0-63 Qh, 64-127 Ql; B rows 0-63 Ph, 64-127 Pl).  Transform
+// thread tt (0 .. KGB_TTHREADS - 1; KGB_TTHREADS a multiple of 8) handles
+// channels 4 (tt & 7) .. + 3 of rows (tt + KGB_TTHREADS v) >> 3.  Returns this thread's 4-bit mask of channels
+// left out as steep.
+template <typename TIn>
+__device__ __forceinline__ uint32_t kgb_tc_transform(const unsigned char *stage, unsigned char *ops, int n,
+                                                     int tt) {
+    constexpr float LH = 1.4426950408889634f;
+    constexpr float SAFE2 = KGB_TC_SAFE * LH;
+    constexpr int KP = 32 * int(sizeof(TIn));          // bytes per staged key row
+    const unsigned char *kb = stage, *gb = stage + KGB_STAGE_G;
+    unsigned char *A = ops, *B = ops + 128 * 128;
+    const int c = tt & 7;
+    // reference: g of the middle live row; steep: g leaves [c - SAFE, c + SAFE]
+    float ref[4], gfirst[4], glast[4];
+    load4(gb + ((n - 1) >> 1) * 128, c, (const float *)nullptr, ref);
+    load4(gb, c, (const float *)nullptr, gfirst);
+    load4(gb + (n - 1) * 128, c, (const float *)nullptr, glast);
+    uint32_t steep = 0;
+    bool keep[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float up = (gfirst[i] - ref[i]) * LH, dn = (ref[i] - glast[i]) * LH;
+        keep[i] = up <= SAFE2 && dn <= SAFE2;          // false for NaN too
+        steep |= keep[i] ? 0u : (1u << i);
+    }
+    static_assert(KGB_TTHREADS % 8 == 0, "a thread keeps its channel group");
+#pragma unroll
+    for (int v = 0; v < (64 * 8 + KGB_TTHREADS - 1) / KGB_TTHREADS; ++v) {
+        if (tt + KGB_TTHREADS * v >= 64 * 8) break;
+        const int r = (tt + KGB_TTHREADS * v) >> 3;
+        float kv[4], gv[4], q[4], pp[4];
+        load4(kb + r * KP, c, (const TIn *)nullptr, kv);
+        load4(gb + r * 128, c, (const float *)nullptr, gv);
+        const bool live = r < n;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // the exponent (g - ref) log2 e: the difference is taken first, so its
+            // error does not grow with |g|
+            const float e = (gv[i] - ref[i]) * LH;
+            const bool on = live && keep[i];           // selected after: 0 * inf would be NaN
+            q[i] = on ? kv[i] * ex2(e) : 0.f;
+            pp[i] = on ? kv[i] * ex2(-e) : 0.f;
+        }
+        uint4 qh, ql, ph, pl;
+        split4(q, qh, ql);
+        split4(pp, ph, pl);
+        const int sw = 16 * (c ^ (r & 7));             // swizzled chunk position (rows r and 64 + r alike)
+        *reinterpret_cast<uint4 *>(A + r * 128 + sw) = qh;
+        *reinterpret_cast<uint4 *>(A + (64 + r) * 128 + sw) = ql;
+        *reinterpret_cast<uint4 *>(B + r * 128 + sw) = ph;
+        *reinterpret_cast<uint4 *>(B + (64 + r) * 128 + sw) = pl;
+    }
+    return steep;
+}
+
+// ------------------------------------------------------------- solve pair
+// The 64-token solve of the A tile (blocks (i, j) at Ab + 256 blk(i, j), pitch
+// 16) by the 64 threads of one pair (tid 0..63, named barrier `bar`).
 template <typename TOut>
-__device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr, TOut *ob, int os, int n, int tid) {
+__device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr, TOut *ob, int os, int n, int tid,
+                                          int bar) {
     const int unit = tid >> 4, warp = tid >> 5, l = tid & 15;
     const int lane = tid & 31, g = lane >> 2, t = lane & 3;
     {
@@ -344,7 +328,7 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
             out_tile_t(ob, os, n, 3, 2, c2, g, t);
         }
     }
-    named_sync64();
+    bar64(bar);
     {   // level B, warp w = column block w of X_BL
         TileA la, lb;
         TileB rb;
@@ -379,63 +363,261 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
     store_upper_zeros(ob, os, n, tid);
 }
 
-template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(KGB_THREADS, 2)
-kda_kgb_kernel(const KgbParams p) {
-    extern __shared__ __align__(128) float sm[];
-    float *kq = sm;                                    // Q slices
-    float *gp = kq + 4 * KGB_SLICE;                    // P slices
-    float *fac = gp + 4 * KGB_SLICE;
-    float *Ab = fac + 4 * KGB_FROWS * 32;
-    float *Xt = Ab + 10 * 256;
-    float *Xr = Xt + 4 * XTS;
-    float *bs = Xr + 4 * XRS;
-    unsigned *steep = reinterpret_cast<unsigned *>(bs + 64);     // [slice][diagonal block]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int nsl = p.K / 32;
-    const bool has_slice = warp < nsl;
+// A tile element (i, j), j <= i (blocks (i/16, j/16) of the lower triangle).
+__device__ __forceinline__ float *at_elem(float *Ab, int i, int j) {
+    return Ab + blk(i >> 4, j >> 4) * 256 + (i & 15) * 16 + (j & 15);
+}
+
+// Solve pair PR: chunk-heads c = PR, PR + KGB_PAIRS, ... from A tile PR.
+template <typename TOut>
+__device__ __forceinline__ void kgb_pair_loop(const KgbParams &p, unsigned char *sm, uint64_t *bars, int PR,
+                                              int pt) {
+    float *Ab = reinterpret_cast<float *>(sm + KGB_OFF_AT) + PR * 2560;
+    float *X = reinterpret_cast<float *>(sm + KGB_OFF_X) + PR * KGB_X_FLOATS;
     const int os = p.H * BT;
-    float *kb = kq + warp * KGB_SLICE, *gb = gp + warp * KGB_SLICE;
-    KgbWalk walk(p, blockIdx.x, gridDim.x);
-    Meta cur = walk.next(p);
-    if (has_slice) kgb_issue<TIn>(p, cur, warp, kb, gb, lane);
-    cp_async_commit();
-    for (;;) {
-        if (!cur.valid) {                              // the same for every thread of the CTA
-            cp_async_wait<0>();
-            break;
-        }
-        float b0 = 0.f, b1 = 0.f;                      // beta of the chunk's rows (warp 0)
-        if (warp == 0) {
-            const TIn *bp = reinterpret_cast<const TIn *>(p.beta) + (int64_t(cur.row0) * p.H + cur.h);
-            if (lane < cur.n) b0 = float(bp[int64_t(lane) * p.H]);
-            if (lane + 32 < cur.n) b1 = float(bp[int64_t(lane + 32) * p.H]);
-        }
-        cp_async_wait<0>();
+    KgbWalk walk(p, int32_t(blockIdx.x) + PR * int32_t(gridDim.x), KGB_PAIRS * int32_t(gridDim.x));
+    Meta m = walk.next(p);
+    for (uint32_t k = 0; m.valid; ++k, m = walk.next(p)) {
+        const bool ok = kgb_wait(bars, BAR_AT_FULL + PR, k & 1, p.err);
+        if (!bar64_and(4 + PR, ok)) break;
+        TOut *ob = reinterpret_cast<TOut *>(p.out) + (int64_t(m.row0) * p.H + m.h) * BT;
+        kgb_solve<TOut>(Ab, X, X + 4 * XTS, ob, os, m.n, pt, 4 + PR);
         __syncwarp();
-        if (has_slice) kgb_transform<TIn>(kb, gb, fac + warp * KGB_FROWS * 32, steep + 4 * warp, cur.n, lane);
-        if (warp == 0) {
-            bs[lane] = b0;
-            bs[lane + 32] = b1;
+        if ((pt & 31) == 0) mbar_arrive(&bars[BAR_AT_EMPTY + PR]);
+    }
+}
+
+// ----------------------------------------------------------------- kernel
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(KGB_THREADS, 1)
+kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    // the swizzled operand buffers need 1024-byte aligned shared addresses
+    unsigned char *sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + KGB_OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + KGB_OFF_TMEM);
+    uint32_t *steep_m = reinterpret_cast<uint32_t *>(sm + KGB_OFF_STEEP);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nsl = p.K / 32;
+    const int32_t G = gridDim.x;
+
+    if (tid == 0) {
+        prefetch_tensormap(&maps.k);
+        prefetch_tensormap(&maps.g);
+        for (int b = 0; b < KGB_NST; ++b) {
+            mbar_init(&bars[BAR_ST_FULL + b], 1);
+            mbar_init(&bars[BAR_ST_EMPTY + b], KGB_TWARPS);
         }
-        __syncthreads();                               // Q, P, factors, beta ready; the last solve is done
-        // blocks blk = warp, warp + 4, warp + 8: (0,0) (2,1) (3,2) | (1,0) (2,2) (3,3) | (1,1) (3,0) | (2,0) (3,1)
-#pragma unroll 1
-        for (int b = warp; b < 10; b += 4) {
-            const int I = b >= 6 ? 3 : b >= 3 ? 2 : b >= 1 ? 1 : 0;
-            const int J = b - I * (I + 1) / 2;
-            kgb_block<TIn>(p, cur, kq, gp, fac, steep, bs, Ab, I, J, nsl, g, t);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[BAR_OPS_FULL + b], KGB_TWARPS);
+            mbar_init(&bars[BAR_OPS_EMPTY + b], 1);
+            mbar_init(&bars[BAR_D_FULL + b], 2);
+            mbar_init(&bars[BAR_D_EMPTY + b], 4);
         }
-        __syncthreads();                               // A complete; the slice buffers are free
-        const Meta nxt = walk.next(p);
-        if (has_slice) kgb_issue<TIn>(p, nxt, warp, kb, gb, lane);
-        cp_async_commit();
-        if (warp < 2) {
-            TOut *ob = reinterpret_cast<TOut *>(p.out) + (int64_t(cur.row0) * p.H + cur.h) * BT;
-            kgb_solve<TOut>(Ab, Xt, Xr, ob, os, cur.n, tid);
+        for (int b = 0; b < KGB_PAIRS; ++b) {
+            mbar_init(&bars[BAR_AT_FULL + b], 4);
+            mbar_init(&bars[BAR_AT_EMPTY + b], 2);
         }
-        cur = nxt;
+        fence_mbar_init();
+    }
+    if (warp == KGB_EW0) {                             // an epilogue warp owns the TMEM allocation
+        tc::tmem_alloc(smem_u32(tmem_slot), KGB_TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------- loader (lane 0)
+        if (lane == 0) {
+            KgbWalk lw(p, blockIdx.x, G);
+            uint32_t lu = 0;
+            for (Meta lm = lw.next(p); lm.valid; lm = lw.next(p)) {
+                int ls = 0;
+                for (; ls < nsl; ++ls, ++lu) {         // slice ls into its staging slot once it is free
+                    const int slot = lu % KGB_NST;
+                    if (!kgb_wait(bars, BAR_ST_EMPTY + slot, ((lu / KGB_NST) & 1) ^ 1, p.err)) break;
+                    kgb_tma_slice<TIn>(maps, lm, ls, sm + KGB_OFF_STAGE + slot * KGB_STAGE_BYTES,
+                                       &bars[BAR_ST_FULL + slot]);
+                }
+                if (ls < nsl) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issue (lane 0)
+        if (lane == 0) {
+            KgbWalk mw(p, blockIdx.x, G);
+            uint32_t mu = 0;
+            bool ok = true;
+            for (uint32_t mc = 0; ok; ++mc) {
+                if (!mw.next(p).valid) break;
+                const int db = mc & 1;
+                // the accumulator buffer's previous chunk-head has been read out
+                ok = kgb_wait(bars, BAR_D_EMPTY + db, ((mc >> 1) & 1) ^ 1, p.err);
+                for (int ms = 0; ok && ms < nsl; ++ms, ++mu) {
+                    const int ob = mu & 1;
+                    if (!(ok = kgb_wait(bars, BAR_OPS_FULL + ob, (mu >> 1) & 1, p.err))) break;
+                    tc::fence_after_sync();
+                    const uint32_t a0 = smem_u32(sm + KGB_OFF_OPS + ob * KGB_OPS_BYTES), b0 = a0 + 128 * 128;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_tf32(tmem + db * 128, tc::sw128_desc(a0 + 32 * kk), tc::sw128_desc(b0 + 32 * kk),
+                                     KGB_IDESC, ms > 0 || kk > 0);
+                    tc::commit(smem_u32(&bars[BAR_OPS_EMPTY + ob]));
+                    if (ms == nsl - 1) {
+                        tc::commit(smem_u32(&bars[BAR_D_FULL + db]));
+                        mbar_arrive(&bars[BAR_D_FULL + db]);     // releases the steep masks
+                    }
+                }
+            }
+        }
+    } else if (warp < 2 + KGB_TWARPS) {
+        // --------------------------------------------------------- transform
+        const int tt = tid - 64;                       // 0 .. KGB_TTHREADS - 1
+        KgbWalk walk(p, blockIdx.x, G);
+        Meta m = walk.next(p);
+        uint32_t u = 0;
+        bool ok = true;
+        for (uint32_t c = 0; m.valid && ok; ++c, m = walk.next(p)) {
+            for (int s = 0; s < nsl; ++s, ++u) {
+                const int slot = u % KGB_NST, ob = u & 1;
+                ok = kgb_wait(bars, BAR_ST_FULL + slot, (u / KGB_NST) & 1, p.err) &&
+                     kgb_wait(bars, BAR_OPS_EMPTY + ob, ((u >> 1) & 1) ^ 1, p.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const uint32_t st = kgb_tc_transform<TIn>(sm + KGB_OFF_STAGE + slot * KGB_STAGE_BYTES,
+                                                          sm + KGB_OFF_OPS + ob * KGB_OPS_BYTES, m.n, tt);
+                if (warp == 2) {                       // lanes 0-7 cover the slice's 8 channel groups
+                    const uint32_t word = __reduce_or_sync(0xffffffffu, st << (4 * (lane & 7)));
+                    if (lane == 0) steep_m[(c & 7) * 4 + s] = word;
+                }
+                fence_proxy_async();                   // operand writes visible to the tensor cores
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[BAR_OPS_FULL + ob]);
+                    mbar_arrive(&bars[BAR_ST_EMPTY + slot]);
+                }
+            }
+        }
+    } else if (warp < KGB_SW0) {
+        // ---------------------------------------------------------- epilogue
+        const int q4 = warp & 3, et = tid - 32 * KGB_EW0;   // TMEM lane quarter (warp w: w % 4), thread 0..127
+        float *sk = reinterpret_cast<float *>(sm + KGB_OFF_SC), *sg = sk + 64;
+        KgbWalk walk(p, blockIdx.x, G);
+        Meta m = walk.next(p);
+        for (uint32_t c = 0; m.valid; ++c, m = walk.next(p)) {
+            const int pr = c % KGB_PAIRS, db = c & 1;
+            float *Ab = reinterpret_cast<float *>(sm + KGB_OFF_AT) + pr * 2560;
+            bool ok = kgb_wait(bars, BAR_AT_EMPTY + pr, ((c / KGB_PAIRS) & 1) ^ 1, p.err);
+            ok = ok && kgb_wait(bars, BAR_D_FULL + db, (c >> 1) & 1, p.err);
+            if (!named_sync_and<3, 128>(ok)) break;
+            tc::fence_after_sync();
+            const uint32_t sbase = (c & 7) * 4;
+            const uint32_t any_steep = (nsl > 0 ? steep_m[sbase] : 0u) | (nsl > 1 ? steep_m[sbase + 1] : 0u) |
+                                       (nsl > 2 ? steep_m[sbase + 2] : 0u) | (nsl > 3 ? steep_m[sbase + 3] : 0u);
+            const uint32_t tq = tmem + db * 128 + (uint32_t(32 * q4) << 16);
+            const int i = 32 * (q4 & 1) + lane;        // chunk row of this thread
+            if (q4 >= 2) {                             // Ql Ph^T: lanes 64..127, columns 0..63
+                float v[4][16];
+#pragma unroll
+                for (int j0 = 0; j0 < 4; ++j0) tc::ld16(tq + 16 * j0, v[j0]);
+                tc::wait_ld();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_D_EMPTY + db]);
+#pragma unroll
+                for (int j0 = 0; j0 < 4; ++j0)
+                    if (16 * j0 <= i)
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4 *>(at_elem(Ab, i, 16 * j0 + e)) =
+                                make_float4(v[j0][e], v[j0][e + 1], v[j0][e + 2], v[j0][e + 3]);
+            }
+            named_sync<3, 128>();                      // partial sums in the A tile
+            if (q4 < 2) {                              // Qh Ph^T + Qh Pl^T, plus the partial
+                const float bi = i < m.n ? float(reinterpret_cast<const TIn *>(p.beta)[(int64_t(m.row0) + i) * p.H + m.h])
+                                         : 0.f;
+#pragma unroll
+                for (int j0 = 0; j0 < 4; ++j0) {
+                    float a[16], b[16];
+                    tc::ld16(tq + 16 * j0, a);
+                    tc::ld16(tq + 64 + 16 * j0, b);
+                    tc::wait_ld();
+                    if (16 * j0 <= i) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            float4 *dst = reinterpret_cast<float4 *>(at_elem(Ab, i, 16 * j0 + e));
+                            const float4 w = *dst;
+                            const float wv[4] = {w.x, w.y, w.z, w.w};
+                            float o[4];
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                const int j = 16 * j0 + e + x;
+                                const float sum = (a[e + x] + b[e + x]) + wv[x];
+                                o[x] = (j < i && i < m.n) ? bi * sum : 0.f;
+                            }
+                            *dst = make_float4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[BAR_D_EMPTY + db]);
+            }
+            if (any_steep != 0u) {
+                // slow path: the steep channels' terms, k_i k_j exp(g_i - g_j), one by one
+                constexpr float L2E = 1.4426950408889634f;
+                const int64_t rs = int64_t(p.H) * p.K;
+                const int ri = et & 63, jh = et >> 6;       // row ri, columns 32 jh .. 32 jh + 31
+                float acc[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+                for (int s = 0; s < nsl; ++s) {
+                    uint32_t mask = steep_m[sbase + s];
+                    while (mask != 0u) {
+                        const int d = 32 * s + __ffs(mask) - 1;
+                        mask &= mask - 1u;
+                        named_sync<3, 128>();                // previous channel's values consumed
+                        if (et < 64) {
+                            const bool live = et < m.n;
+                            const int64_t off = (int64_t(m.row0) + et) * rs + int64_t(m.h) * p.K + d;
+                            sk[et] = live ? float(reinterpret_cast<const TIn *>(p.k)[off]) : 0.f;
+                            sg[et] = live ? p.g[off] : 0.f;
+                        }
+                        named_sync<3, 128>();
+                        const float ki = sk[ri], gi = sg[ri];
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            const int j = 32 * jh + x;
+                            if (j < ri) acc[x] = fmaf(ki * sk[j], ex2((gi - sg[j]) * L2E), acc[x]);
+                        }
+                    }
+                }
+                named_sync<3, 128>();                    // the partial-sum pass is complete
+                if (ri < m.n) {
+                    const float bi = float(reinterpret_cast<const TIn *>(p.beta)[(int64_t(m.row0) + ri) * p.H + m.h]);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        const int j = 32 * jh + x;
+                        if (j < ri) *at_elem(Ab, ri, j) += bi * acc[x];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[BAR_AT_FULL + pr]);     // releases the A tile
+        }
+    } else {
+        // -------------------------------------------------------- solve pairs
+        const int pr = (warp - KGB_SW0) >> 1, pt = tid - 32 * KGB_SW0 - 64 * pr;   // pair, thread 0..63 in it
+        kgb_pair_loop<TOut>(p, sm, bars, pr, pt);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == KGB_EW0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, KGB_TMEM_COLS);
     }
 }
 

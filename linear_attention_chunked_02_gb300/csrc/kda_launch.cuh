@@ -77,7 +77,7 @@ cudaError_t launch_in(int mode, int out_dtype, const Maps &maps, const Params &p
 // ------------------------------------------------ 16- and 32-token chunks
 template <int CBT, typename TIn, typename TOut>
 struct SmallKernel {
-    static constexpr int SLOTS = CBT == 16 ? 4 : 2;   // chunk-heads a CTA works on at once
+    static constexpr int SLOTS = CBT == 16 ? BT16_SLOTS : 2;   // chunk-heads a CTA works on at once
     static void (*fn())(SmallParams) { return CBT == 16 ? kda_bt16_kernel<TIn, TOut> : kda_bt32_kernel<TIn, TOut>; }
     static int blocks_per_sm(int device, cudaError_t &err) {
         static std::mutex mu;
@@ -148,24 +148,26 @@ struct KgbKernel {
         cached[device] = occ > 0 ? occ : 1;
         return cached[device];
     }
-    static cudaError_t launch(const KgbParams &p, int device, int num_sms, cudaStream_t stream) {
+    static cudaError_t launch(const KgbMaps &maps, const KgbParams &p, int device, int num_sms,
+                              cudaStream_t stream) {
         cudaError_t err;
         const int occ = blocks_per_sm(device, err);
         if (err != cudaSuccess) return err;
         long long grid = (long long)num_sms * occ;
         if (grid > p.n_tasks) grid = p.n_tasks;
         if (grid < 1) return cudaSuccess;
-        kda_kgb_kernel<TIn, TOut><<<(unsigned)grid, KGB_THREADS, KGB_BYTES, stream>>>(p);
+        kda_kgb_kernel<TIn, TOut><<<(unsigned)grid, KGB_THREADS, KGB_BYTES, stream>>>(maps, p);
         return cudaGetLastError();
     }
 };
 
 template <typename TIn>
-cudaError_t launch_kgb_in(int out_dtype, const KgbParams &p, int device, int num_sms, cudaStream_t stream) {
+cudaError_t launch_kgb_in(int out_dtype, const KgbMaps &maps, const KgbParams &p, int device, int num_sms,
+                          cudaStream_t stream) {
     switch (out_dtype) {
-        case 0: return KgbKernel<TIn, float>::launch(p, device, num_sms, stream);
-        case 1: return KgbKernel<TIn, __nv_bfloat16>::launch(p, device, num_sms, stream);
-        default: return KgbKernel<TIn, __half>::launch(p, device, num_sms, stream);
+        case 0: return KgbKernel<TIn, float>::launch(maps, p, device, num_sms, stream);
+        case 1: return KgbKernel<TIn, __nv_bfloat16>::launch(maps, p, device, num_sms, stream);
+        default: return KgbKernel<TIn, __half>::launch(maps, p, device, num_sms, stream);
     }
 }
 
@@ -176,8 +178,8 @@ cudaError_t launch_f16(int mode, int out_dtype, const Maps &, const Params &, in
 cudaError_t launch_small_f32(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
 cudaError_t launch_small_bf16(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
 cudaError_t launch_small_f16(int bt, int out_dtype, const SmallParams &, int, int, cudaStream_t);
-cudaError_t launch_kgb_f32(int out_dtype, const KgbParams &, int, int, cudaStream_t);
-cudaError_t launch_kgb_bf16(int out_dtype, const KgbParams &, int, int, cudaStream_t);
-cudaError_t launch_kgb_f16(int out_dtype, const KgbParams &, int, int, cudaStream_t);
+cudaError_t launch_kgb_f32(int out_dtype, const KgbMaps &, const KgbParams &, int, int, cudaStream_t);
+cudaError_t launch_kgb_bf16(int out_dtype, const KgbMaps &, const KgbParams &, int, int, cudaStream_t);
+cudaError_t launch_kgb_f16(int out_dtype, const KgbMaps &, const KgbParams &, int, int, cudaStream_t);
 
 }  // namespace kda

@@ -67,6 +67,22 @@ struct SlotWalk {
     }
 };
 
+// cu_seqlens entries cached in shared memory by the short-chunk kernels
+// (packed batches of up to 511 requests)
+constexpr int SMALL_CU_CAP = 512;
+
+// p with cu pointing to a shared-memory copy of cu_seqlens when it fits (every
+// thread of the CTA calls this; it ends with a CTA barrier in that case).
+__device__ __forceinline__ SmallParams with_cached_cu(const SmallParams &p, int32_t *cu_s, int tid) {
+    SmallParams ps = p;
+    if (p.cu != nullptr && p.nseq < SMALL_CU_CAP) {
+        for (int i = tid; i <= p.nseq; i += NTHREADS) cu_s[i] = __ldg(p.cu + i);
+        ps.cu = cu_s;
+        __syncthreads();
+    }
+    return ps;
+}
+
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
@@ -93,51 +109,89 @@ __device__ __forceinline__ void widen_blocks(const TIn *src, int b_hi, float *ds
 }
 
 // ------------------------------------------------------------ 16 tokens
-// Ring stage of one unit: the 16x16 tile, row-major, pitch 16 elements.  Lane
+// A group of 8 lanes solves one chunk-head; lane l owns columns 2l and 2l + 1,
+// so every row of A it loads serves two forward substitutions.
+constexpr int BT16_LANES = 8;
+constexpr int BT16_SLOTS = NTHREADS / BT16_LANES;      // chunk-heads a CTA works on at once
+
+// Ring stage of one slot: the 16x16 tile, row-major, pitch 16 elements.  Lane
 // l copies 16 bytes of rows i0, i0 + DI, ... (i0 = l / PER_ROW).
 template <typename TIn>
 __device__ __forceinline__ void issue16(const SmallParams &p, const Meta &m, TIn *stage, int l) {
     constexpr int VEC = Elt<TIn>::VEC;
     constexpr int PER_ROW = 16 / VEC;                  // 16-byte copies per row
-    constexpr int DI = 16 / PER_ROW;                   // rows between a lane's copies
+    constexpr int DI = BT16_LANES / PER_ROW;           // rows between a lane's copies
     if (!m.valid) return;
     const int rs = p.H * 16;                           // row stride (elements)
     const int i0 = l / PER_ROW, k = (l % PER_ROW) * VEC;
     const TIn *src = reinterpret_cast<const TIn *>(p.A) + (int64_t(m.row0) * rs + m.h * 16) + (i0 * rs + k);
     TIn *dst = stage + i0 * 16 + k;
 #pragma unroll
-    for (int it = 0; it < PER_ROW; ++it) {
+    for (int it = 0; it < 16 / DI; ++it) {
         const bool live = i0 + DI * it < m.n;
         cp_async16(dst + DI * 16 * it, live ? src : p.A, live ? 16u : 0u);
         src += DI * rs;
     }
 }
 
-// 16-token chunks: unit u of CTA b solves chunk-heads 4b + u, 4b + u + 4 grid, ...
+// Forward substitution for columns j and j + 1 of the 16x16 unit-lower inverse:
+// the diag_invert recurrence, each row of `a` loaded once for both columns.
+__device__ __forceinline__ void diag_invert2(const float *a, int ap, int j, float (&x)[16], float (&y)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = (i == j) ? 1.f : 0.f;
+        y[i] = (i == j + 1) ? 1.f : 0.f;
+    }
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+        float s = 0.f, u = 0.f;
+#pragma unroll
+        for (int kq = 0; kq < (i + 3) / 4; ++kq) {
+            const float4 v = *reinterpret_cast<const float4 *>(a + i * ap + 4 * kq);
+            if (4 * kq + 0 < i) { s = fmaf(-v.x, x[4 * kq + 0], s); u = fmaf(-v.x, y[4 * kq + 0], u); }
+            if (4 * kq + 1 < i) { s = fmaf(-v.y, x[4 * kq + 1], s); u = fmaf(-v.y, y[4 * kq + 1], u); }
+            if (4 * kq + 2 < i) { s = fmaf(-v.z, x[4 * kq + 2], s); u = fmaf(-v.z, y[4 * kq + 2], u); }
+            if (4 * kq + 3 < i) { s = fmaf(-v.w, x[4 * kq + 3], s); u = fmaf(-v.w, y[4 * kq + 3], u); }
+        }
+        x[i] = (i > j) ? s : x[i];
+        y[i] = (i > j + 1) ? u : y[i];
+    }
+}
+
+// two consecutive output elements
+__device__ __forceinline__ void put2(float *p, float a, float b) { *reinterpret_cast<float2 *>(p) = make_float2(a, b); }
+template <typename TOut>
+__device__ __forceinline__ void put2(TOut *p, float a, float b) {
+    *reinterpret_cast<uint32_t *>(p) = pack2(a, b, (TOut *)nullptr);
+}
+
+// 16-token chunks: slot u of CTA b solves chunk-heads 8b + u, 8b + u + 8 grid, ...
 template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(NTHREADS, 14)
+__global__ void __launch_bounds__(NTHREADS, 10)
 kda_bt16_kernel(const SmallParams p) {
     constexpr int S = SMALL_STAGES;
     constexpr bool WIDEN = sizeof(TIn) == 2;
-    __shared__ __align__(16) TIn ring[4][S][256];
-    __shared__ __align__(16) float af[WIDEN ? 4 : 1][WIDEN ? 256 : 4];   // widened tile (16-bit input)
-    const int tid = threadIdx.x, unit = tid >> 4, l = tid & 15;
-    const unsigned mask = 0xffffu << (16 * (unit & 1));
-    const int32_t slots = gridDim.x * 4;
-    const int32_t q0 = blockIdx.x * 4 + unit;
+    __shared__ __align__(16) TIn ring[BT16_SLOTS][S][256];
+    __shared__ __align__(16) float af[WIDEN ? BT16_SLOTS : 1][WIDEN ? 256 : 4];   // widened tile (16-bit input)
+    __shared__ int32_t cu_s[SMALL_CU_CAP];
+    const int tid = threadIdx.x, slot = tid / BT16_LANES, l = tid % BT16_LANES;
+    const unsigned mask = 0xffu << (BT16_LANES * (slot & 3));
+    const int32_t slots = gridDim.x * BT16_SLOTS;
+    const int32_t q0 = blockIdx.x * BT16_SLOTS + slot;
     const int rs = p.H * 16;                 // row stride (elements); H * 16 * 16 < 2^31
-    SlotWalk<16> walk(p, q0, slots);
+    const SmallParams ps = with_cached_cu(p, cu_s, tid);
+    SlotWalk<16> walk(ps, q0, slots);
     // metas of the chunk-heads in the ring: m[0] is computed next
     Meta m[S];
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
-        m[s] = walk.next(p);
-        issue16<TIn>(p, m[s], ring[unit][s], l);
+        m[s] = walk.next(ps);
+        issue16<TIn>(p, m[s], ring[slot][s], l);
         cp_async_commit();
     }
     for (int k = 0;; ++k) {
-        m[S - 1] = walk.next(p);
-        issue16<TIn>(p, m[S - 1], ring[unit][(k + S - 1) % S], l);
+        m[S - 1] = walk.next(ps);
+        issue16<TIn>(p, m[S - 1], ring[slot][(k + S - 1) % S], l);
         cp_async_commit();
         if (!m[0].valid) {                 // later chunk-heads are past the end too (nothing issued)
             cp_async_wait<0>();
@@ -145,22 +199,22 @@ kda_bt16_kernel(const SmallParams p) {
         }
         cp_async_wait<S - 1>();
         __syncwarp(mask);
-        const float *a = reinterpret_cast<const float *>(ring[unit][k % S]);
+        const float *a = reinterpret_cast<const float *>(ring[slot][k % S]);
         if constexpr (WIDEN) {
-            widen_blocks(ring[unit][k % S], 0, af[unit], 1, l, 16);
+            widen_blocks(ring[slot][k % S], 0, af[slot], 1, l, BT16_LANES);
             __syncwarp(mask);
-            a = af[unit];
+            a = af[slot];
         }
-        float x[16];
-        diag_invert(a, 16, l, x);
-        TOut *op = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * rs + (m[0].h * 16 + l));
+        float x[16], y[16];
+        diag_invert2(a, 16, 2 * l, x, y);
+        TOut *op = reinterpret_cast<TOut *>(p.out) + (int64_t(m[0].row0) * rs + (m[0].h * 16 + 2 * l));
         if (m[0].n == 16) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i, op += rs) put1(op, x[i]);
+            for (int i = 0; i < 16; ++i, op += rs) put2(op, x[i], y[i]);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i, op += rs)
-                if (i < m[0].n) put1(op, x[i]);
+                if (i < m[0].n) put2(op, x[i], y[i]);
         }
         __syncwarp(mask);                  // stage k % S is refilled next
 #pragma unroll
@@ -214,22 +268,24 @@ kda_bt32_kernel(const SmallParams p) {
     __shared__ __align__(16) float af[2][AX ? 512 : 4];   // widened diagonal blocks (16-bit input)
     __shared__ __align__(16) float xt[2][256];    // X00^T, pitch XTP
     __shared__ __align__(16) float xr[2][XRS];    // -X11, pitch XRP
+    __shared__ int32_t cu_s[SMALL_CU_CAP];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int half = (tid >> 4) & 1, l = tid & 15;
     const int g = lane >> 2, t = lane & 3;
     const int32_t slots = gridDim.x * 2;
     const int32_t q0 = blockIdx.x * 2 + warp;
     const int os = p.H * 32;
-    SlotWalk<32> walk(p, q0, slots);
+    const SmallParams ps = with_cached_cu(p, cu_s, tid);
+    SlotWalk<32> walk(ps, q0, slots);
     Meta m[S];
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
-        m[s] = walk.next(p);
+        m[s] = walk.next(ps);
         issue32<TIn>(p, m[s], ring[warp][s], lane);
         cp_async_commit();
     }
     for (int k = 0;; ++k) {
-        m[S - 1] = walk.next(p);
+        m[S - 1] = walk.next(ps);
         issue32<TIn>(p, m[S - 1], ring[warp][(k + S - 1) % S], lane);
         cp_async_commit();
         if (!m[0].valid) {                 // later chunk-heads are past the end too (nothing issued)

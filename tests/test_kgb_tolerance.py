@@ -1,24 +1,23 @@
 """Where the fused path's tolerance comes from (CPU only).
 
-The fused kernel builds each chunk's matrix in FP32 from keys, decays and betas.
-Per 16-row block I with first row rI and last live row eI:
+The fused kernel builds each chunk's matrix in FP32 from keys, decays and betas
+with one reference value c_d per channel (g of the chunk's middle live row):
 
-* Q_I = k exp(g - g_rI) and P_I = k exp(g_eI - g): every exponent is <= 0 for
-  a non-increasing g, so neither factor can overflow;
-* block (I, J), I > J: (Q_I * exp(g_rI - g_eJ)) P_J^T, again with a
-  non-positive exponent;
-* diagonal block (I, I): (Q_I * exp(g_rI - g_eI)) P_I^T for the channels whose
-  decay over the block stays within a safe span; the channels that fall
-  further are left out of that product and their terms are added one by one as
-  k_i k_j exp(g_i - g_j).
+* Q = k 2^{(g - c) log2 e} and P = k 2^{(c - g) log2 e}, the difference g - c
+  taken first and then scaled, so the exponent's error grows with its size but
+  not with |g|;
+* A = beta * strict_lower(Q P^T), the product taken in split TF32 on the tensor
+  cores (Qh Ph^T + Qh Pl^T + Ql Ph^T, hi parts truncated to TF32, FP32 sums);
+* a channel whose g leaves [c - 48, c + 48] over the chunk's live rows is left
+  out of the product and its terms k_i k_j exp(g_i - g_j) are added one by one.
 
 This test runs that arithmetic in numpy float32 and compares it with the fp64
 oracle on the same rounded inputs: the worst error must sit far inside the
 2e-5 * (1 + |ref|) the GPU parity tests use for every input dtype, on KDA
 decays, on no decay, and on steep decays (per-token drops of 3 to 20 nats and
-cliffs of 100 nats, so that blocks fall by far more than FP32's exponent range).
-A planted copy that factors through the block's first row alone (the form that
-overflows) must fail on the steep inputs.
+cliffs of 100 nats), and on decays that take the factors' exponents near the
+largest the product accepts.  A planted copy without the steep channels' slow
+path must fail on the steep inputs.
 """
 import numpy as np
 import pytest
@@ -26,49 +25,38 @@ import pytest
 import kda_inputs as ki
 import oracle
 
-BT, BS = 64, 16
-SAFE_SPAN = 32.0          # nats of decay over a diagonal block that its product still takes
+BT = 64
+SAFE = 48.0               # nats of g from the channel's reference that the product takes
+L2E = 1.4426950408889634
 
 
-def _fp32_construction(k, g, beta, n, first_row_only=False):
-    """FP32 A [n, n] of one chunk-head by the block-reference factorisation."""
+def _tf32(x):
+    """Truncate float32 values to TF32 (10 explicit mantissa bits)."""
+    return (np.asarray(x, np.float32).view(np.uint32) & np.uint32(0xFFFFE000)).view(np.float32)
+
+
+def _fp32_construction(k, g, beta, n, steep_path=True):
+    """FP32 A [n, n] of one chunk-head by the single-reference factorisation."""
     f32 = np.float32
-    K = k.shape[1]
-    kp = np.zeros((BT, K), f32)
-    gp = np.zeros((BT, K), f32)
-    kp[:n], gp[:n] = k, g
-    A = np.zeros((BT, BT), f32)
-    live = (np.arange(BT) < n)[:, None]
+    k = k.astype(f32)
+    g = g.astype(f32)
+    ref = g[(n - 1) // 2]
+    keep = ((g[0] - ref) * f32(L2E) <= f32(SAFE * L2E)) & ((ref - g[n - 1]) * f32(L2E) <= f32(SAFE * L2E))
+    if not steep_path:
+        keep = np.ones_like(keep)
     with np.errstate(over="ignore", under="ignore", invalid="ignore"):
-        for I in range(4):
-            rI = BS * I
-            if rI >= n:
-                continue
-            eI = min(rI + BS - 1, n - 1)
-            QI = np.where(live[rI:rI + BS], kp[rI:rI + BS] * np.exp(gp[rI:rI + BS] - gp[rI]), 0).astype(f32)
-            for J in range(I + 1):
-                rJ = BS * J
-                eJ = min(rJ + BS - 1, n - 1)
-                if first_row_only:          # P_J = k exp(g_rJ - g): a positive exponent
-                    PJ = kp[rJ:rJ + BS] * np.exp(gp[rJ] - gp[rJ:rJ + BS])
-                    f = np.exp(gp[rI] - gp[rJ]) if I > J else np.ones(K, f32)
-                else:
-                    PJ = kp[rJ:rJ + BS] * np.exp(gp[eJ] - gp[rJ:rJ + BS])
-                    f = np.exp(gp[rI] - gp[eJ])
-                PJ = np.where(live[rJ:rJ + BS], PJ, 0).astype(f32)
-                f = f.astype(f32)
-                steep = np.zeros(K, bool)
-                if I == J and not first_row_only:
-                    steep = (gp[rI] - gp[eI]) > SAFE_SPAN
-                    f = np.where(steep, f32(0), f).astype(f32)
-                blk = (QI * f).astype(f32) @ PJ.T
-                for d in np.nonzero(steep)[0]:          # the steep channels, term by term
-                    kc, gc = kp[rI:rI + BS, d], gp[rI:rI + BS, d]
-                    t = (kc[:, None] * kc[None, :]) * np.exp(gc[:, None] - gc[None, :]).astype(f32)
-                    ok = live[rI:rI + BS] & live[rI:rI + BS].T & np.tri(BS, k=-1, dtype=bool)
-                    blk = (blk + np.where(ok, t, 0)).astype(f32)
-                A[rI:rI + BS, rJ:rJ + BS] = blk
-    return (np.tril(A, -1)[:n, :n] * np.asarray(beta[:n], f32)[:, None]).astype(f32)
+        e = ((g - ref).astype(f32) * f32(L2E)).astype(f32)
+        Q = np.where(keep, k * np.exp2(e), 0).astype(f32)
+        P = np.where(keep, k * np.exp2(-e), 0).astype(f32)
+        Qh, Ph = _tf32(Q), _tf32(P)
+        Ql, Pl = _tf32(Q - Qh), _tf32(P - Ph)
+        D = (Qh.astype(np.float64) @ Ph.T.astype(np.float64) + Qh.astype(np.float64) @ Pl.T.astype(np.float64)
+             + Ql.astype(np.float64) @ Ph.T.astype(np.float64)).astype(f32)
+        for dch in np.nonzero(~keep)[0]:
+            kc, gc = k[:, dch], g[:, dch]
+            D = (D + (kc[:, None] * kc[None, :]) * np.exp((gc[:, None] - gc[None, :]).astype(f32)).astype(f32)
+                 ).astype(f32)
+    return (np.tril(D, -1) * np.asarray(beta[:n], f32)[:, None]).astype(f32)
 
 
 def _fp32_solve(A):
@@ -81,9 +69,9 @@ def _fp32_solve(A):
     return X
 
 
-def _worst(kind, in_dtype, first_row_only=False):
+def _worst(kind, in_dtype, **kw):
     wl = ki.Workload("tol", "packed", H=3, in_dtype=in_dtype, out_dtype="f32", seed=5,
-                     seqlens=(64, 64, 40), kind=kind)
+                     seqlens=(64, 64, 40, 7), kind=kind)
     x = ki.build_kgb(wl)
     k, g, b = (oracle.to_f64(t) for t in (x.k, x.g, x.beta))
     ref = oracle.get().solve_kgb(k, g, b, x.cu_seqlens.numpy())[0]
@@ -91,9 +79,8 @@ def _worst(kind, in_dtype, first_row_only=False):
     with np.errstate(invalid="ignore", over="ignore"):
         for row0, n in x.chunks():
             for h in range(x.H):
-                A = _fp32_construction(k[0, row0:row0 + n, h].astype(np.float32),
-                                       g[0, row0:row0 + n, h].astype(np.float32), b[0, row0:row0 + n, h], n,
-                                       first_row_only)
+                A = _fp32_construction(k[0, row0:row0 + n, h], g[0, row0:row0 + n, h], b[0, row0:row0 + n, h], n,
+                                       **kw)
                 X = _fp32_solve(A)
                 R = ref[row0:row0 + n, h, :n]
                 err = np.abs(X - R) / (1 + np.abs(R))
@@ -108,5 +95,25 @@ def test_fp32_construction_is_far_inside_the_tolerance(kind, in_dtype):
     assert worst <= 2e-5 / 100, worst
 
 
-def test_first_row_factorisation_fails_on_steep_decays():
-    assert _worst("steep", "f32", first_row_only=True) > 2e-5
+def test_steep_channels_need_their_slow_path():
+    assert _worst("steep", "f32", steep_path=False) > 2e-5
+
+
+def test_decays_near_the_safe_span():
+    """Every channel decaying about 1.45 nats per token: g reaches about 46 nats from
+    the reference at the chunk's ends, near the span the product takes (some
+    channels just past it take the slow path), so the factors carry exponents
+    near their largest."""
+    rng = np.random.default_rng(1)
+    orc = oracle.get()
+    worst = 0.0
+    for _ in range(4):
+        k = rng.standard_normal((64, 128))
+        k /= np.linalg.norm(k, axis=1, keepdims=True)
+        k = k.astype(np.float32).astype(np.float64)
+        g = (-1.45 * np.arange(64)[:, None] * rng.uniform(0.9, 1.1, (1, 128))).astype(np.float32).astype(np.float64)
+        b = (1 / (1 + np.exp(-rng.standard_normal(64)))).astype(np.float32).astype(np.float64)
+        ref = orc.solve_kgb(k[None, :, None], g[None, :, None], b[None, :, None])[0][:, 0, :]
+        X = _fp32_solve(_fp32_construction(k, g, b, 64))
+        worst = max(worst, float(np.max(np.abs(X - ref) / (1 + np.abs(ref)))))
+    assert worst <= 2e-5 / 100, worst

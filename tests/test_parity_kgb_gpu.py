@@ -150,6 +150,24 @@ def test_kgb_steep_decays_full_size(kda, orc, out_dtype):
     check(x, run(kda, x, out_dtype), reference(orc, x), out_dtype, f"steep full size -> {out_dtype}")
 
 
+def test_kgb_decays_near_the_safe_span(kda, orc):
+    """Every channel decaying about 1.45 nats per token, so that g reaches about 46
+    nats from the chunk's middle at its ends: the tensor-core product's factors
+    carry exponents near the largest it accepts (channels just past it take the
+    slow path)."""
+    T, H, K = 200, 3, 128
+    rng = np.random.default_rng(17)
+    k = rng.standard_normal((1, T, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    t = np.arange(T) % 64
+    g = -1.45 * t[None, :, None, None] * rng.uniform(0.9, 1.1, (1, 1, H, K))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((1, T, H))))
+    wl = ki.Workload("near", "dense", H=H, in_dtype="f32", out_dtype="f32", seed=0, B=1, T=T)
+    x = ki.KgbInput(wl, torch.from_numpy(k.astype(np.float32)), torch.from_numpy(g.astype(np.float32)),
+                    torch.from_numpy(beta.astype(np.float32)), None, [T])
+    check(x, run(kda, x), reference(orc, x), F32, "near the safe span")
+
+
 def test_kgb_residual(kda, orc):
     x = ki.build_kgb(ki.Workload("res", "packed", H=4, in_dtype="f32", out_dtype="f32", seed=31,
                                  seqlens=(64, 100, 33)))
@@ -215,3 +233,7 @@ def test_kgb_argument_errors(kda):
         kda.solve_tril_kgb(k[..., :16].contiguous(), g[..., :16].contiguous(), b)
     assert e.value.status == 2
 
+
+def test_kgb_no_device_error_recorded(kda):
+    """No bounded wait of the fused kernel ran out during this module."""
+    assert kda.device_error(0) == 0
