@@ -587,6 +587,25 @@ __device__ __forceinline__ void mma_tile(TileC &c, const TileA &a, const TileB &
         }
 }
 
+// c += P Q and d += P R, interleaved (two independent accumulator chains; each
+// accumulates in the same order as mma_tile).
+template <bool B_EXACT>
+__device__ __forceinline__ void mma_tile2(TileC &c, TileC &d, const TileA &a, const TileB &q, const TileB &r) {
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            mma8(c.c[nt], a.l[ks], q.h[ks][nt][0], q.h[ks][nt][1]);
+            mma8(d.c[nt], a.l[ks], r.h[ks][nt][0], r.h[ks][nt][1]);
+            if (!B_EXACT) {
+                mma8(c.c[nt], a.h[ks], q.l[ks][nt][0], q.l[ks][nt][1]);
+                mma8(d.c[nt], a.h[ks], r.l[ks][nt][0], r.l[ks][nt][1]);
+            }
+            mma8(c.c[nt], a.h[ks], q.h[ks][nt][0], q.h[ks][nt][1]);
+            mma8(d.c[nt], a.h[ks], r.h[ks][nt][0], r.h[ks][nt][1]);
+        }
+}
+
 // C tile holding Y^T -> output block (bi, bj) of the chunk (rows below n only).
 template <int CBT = BT, typename TOut>
 __device__ __forceinline__ void out_tile_t(TOut *ob, int os, int n, int bi, int bj, const TileC &c, int g, int t) {
@@ -832,18 +851,21 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
                 right4a(rb, a3.p, a3.pitch, g, t);
                 mma_tile<AX>(ct3, la, rb);
             }
+            // X_2w^T = T_2w^T (-X22)^T and the first term of X_3w^T, T_2w^T (-X32)^T,
+            // as two interleaved chains; then + T_3w^T (-X33)^T
             left_regs(la, ct2);
             left_regs(lb, ct3);
+            TileB rb3;
+            TileC cy;
             right2(rb, Xr + XR_22 * XRS, XRP, g, t);
+            right2(rb3, Xr + XR_32 * XRS, XRP, g, t);
             zero(cx);
-            mma_tile<false>(cx, la, rb);
+            zero(cy);
+            mma_tile2<false>(cx, cy, la, rb, rb3);
             out_tile_t(ob, os, m.n, 2, warp, cx, g, t);
-            right2(rb, Xr + XR_32 * XRS, XRP, g, t);
-            zero(cx);
-            mma_tile<false>(cx, la, rb);
             right2(rb, Xr + XR_33 * XRS, XRP, g, t);
-            mma_tile<false>(cx, lb, rb);
-            out_tile_t(ob, os, m.n, 3, warp, cx, g, t);
+            mma_tile<false>(cy, lb, rb);
+            out_tile_t(ob, os, m.n, 3, warp, cy, g, t);
         }
     }
 }

@@ -349,16 +349,17 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
         }
         left_regs(la, ct2);
         left_regs(lb, ct3);
+        TileB rb3;
+        TileC cy;
         right2(rb, Xr + XR_22 * XRS, XRP, g, t);
+        right2(rb3, Xr + XR_32 * XRS, XRP, g, t);
         zero(cx);
-        mma_tile<false>(cx, la, rb);
+        zero(cy);
+        mma_tile2<false>(cx, cy, la, rb, rb3);
         out_tile_t(ob, os, n, 2, warp, cx, g, t);
-        right2(rb, Xr + XR_32 * XRS, XRP, g, t);
-        zero(cx);
-        mma_tile<false>(cx, la, rb);
         right2(rb, Xr + XR_33 * XRS, XRP, g, t);
-        mma_tile<false>(cx, lb, rb);
-        out_tile_t(ob, os, n, 3, warp, cx, g, t);
+        mma_tile<false>(cy, lb, rb);
+        out_tile_t(ob, os, n, 3, warp, cy, g, t);
     }
     store_upper_zeros(ob, os, n, tid);
 }
