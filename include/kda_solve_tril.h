@@ -144,8 +144,10 @@ KDA_API kda_path_t kda_solve_tril_select(int64_t B, int64_t T, int32_t H, int32_
  *   workspace_bytes  its size.
  *   stream      cudaStream_t to launch on.
  *
- * Computes in FP32 (FFMA); result within 2e-5*(1+|ref|) of the exact inverse
- * of the FP32-widened input on the specified workloads.
+ * Computes in FP32: FP32 FMA for the diagonal inverses, split-TF32 tensor-core
+ * products (three TF32 products per FP32 product, FP32 accumulation) for the
+ * merge; result within 2e-5*(1+|ref|) of the exact inverse of the
+ * FP32-widened input on the specified workloads.
  */
 KDA_API kda_status_t kda_solve_tril(const void *A, void *Ai, const int32_t *cu_seqlens,
                             int32_t num_seqs, int64_t B, int64_t T, int32_t H,
@@ -266,9 +268,11 @@ KDA_API kda_status_t kda_solve_tril_bt(const void *A, void *Ai, const int32_t *c
  *               only differences inside a chunk are used, so g may restart at
  *               chunk starts or run on.  16-byte aligned.  g must not increase
  *               along a chunk (each token's decay is at most 1); how far it
- *               falls is not limited.  Channels that fall by more than 32
- *               within a 16-token block take a slower path for that block
- *               (KDA's decays, about one per token, do not).
+ *               falls is not limited.  A channel whose g, over the chunk's
+ *               live rows, lies more than 48 from its value at the chunk's
+ *               middle live row (row (n - 1) / 2 of a chunk of n rows) takes
+ *               a slower path for that chunk-head (KDA's decays, about one
+ *               per token, do not).
  *   beta        device, [B, T, H] of in_dtype, aligned to its element size.
  *   Ai          device, [B, T, H, 64] of out_dtype, 16-byte aligned; must not
  *               overlap k, g or beta.

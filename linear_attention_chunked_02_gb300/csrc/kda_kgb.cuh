@@ -36,7 +36,7 @@
 //     accumulator.  Issuing a TMA or tensor-core instruction holds the issuing
 //     warp for a while, so the two streams run on warps of their own;
 //   * warps 2-7 (transform): each slice of the staging ring into the four TF32
-//     operand parts in a 128-byte-swizzled buffer (two-slice ring); every warp
+//     operand parts in a 128-byte-swizzled buffer (three-slice ring); every warp
 //     signals the MMA warp on its own mbarrier arrival, without a group barrier;
 //   * warps 8-11 (epilogue): tcgen05.ld of the accumulator rows (warp w reads
 //     TMEM lanes 32 (w % 4) .. + 31), the three quadrants added, beta and the
@@ -93,13 +93,17 @@ constexpr float KGB_TC_SAFE = 48.0f;
 constexpr int KGB_NST = 4;
 constexpr int KGB_STAGE_BYTES = 2 * 64 * 128;      // k box (<= 8 KiB), then the g box at +8 KiB
 constexpr int KGB_STAGE_G = 64 * 128;
+// ring of TF32 operand buffers (one slice each): the transform of slice u waits
+// only for the MMAs of slice u - KGB_NOPS, so the slowest transform warp and the
+// MMA latency stay off the transform's path
+constexpr int KGB_NOPS = 3;
 
 // mbarriers
 constexpr int BAR_ST_FULL = 0;                     // [KGB_NST]
 constexpr int BAR_ST_EMPTY = KGB_NST;              // [KGB_NST]
-constexpr int BAR_OPS_FULL = 2 * KGB_NST;          // [2]
-constexpr int BAR_OPS_EMPTY = BAR_OPS_FULL + 2;    // [2]
-constexpr int BAR_D_FULL = BAR_OPS_EMPTY + 2;      // [2]
+constexpr int BAR_OPS_FULL = 2 * KGB_NST;          // [KGB_NOPS]
+constexpr int BAR_OPS_EMPTY = BAR_OPS_FULL + KGB_NOPS;   // [KGB_NOPS]
+constexpr int BAR_D_FULL = BAR_OPS_EMPTY + KGB_NOPS;     // [2]
 constexpr int BAR_D_EMPTY = BAR_D_FULL + 2;        // [2]
 constexpr int BAR_AT_FULL = BAR_D_EMPTY + 2;       // [KGB_PAIRS]
 constexpr int BAR_AT_EMPTY = BAR_AT_FULL + KGB_PAIRS;   // [KGB_PAIRS]
@@ -111,9 +115,9 @@ constexpr int KGB_OFF_TMEM = KGB_NBARS * 8;        // TMEM base address written 
 // steep-channel masks [8 chunk-heads][4 slices]: a ring deep enough that the
 // transform cannot overwrite a chunk-head's masks before its epilogue is done
 constexpr int KGB_OFF_STEEP = KGB_OFF_TMEM + 64;
-constexpr int KGB_OFF_OPS = 1024;                  // [2 slices] {A: 128 x 128 B, B: 128 x 128 B}
+constexpr int KGB_OFF_OPS = 1024;                  // [KGB_NOPS slices] {A: 128 x 128 B, B: 128 x 128 B}
 constexpr int KGB_OPS_BYTES = 2 * 128 * 128;
-constexpr int KGB_OFF_STAGE = KGB_OFF_OPS + 2 * KGB_OPS_BYTES;   // [KGB_NST] staging slots
+constexpr int KGB_OFF_STAGE = KGB_OFF_OPS + KGB_NOPS * KGB_OPS_BYTES;   // [KGB_NST] staging slots
 constexpr int KGB_OFF_AT = KGB_OFF_STAGE + KGB_NST * KGB_STAGE_BYTES;  // [pairs] A tile, 10 blocks of 16 x 16
 constexpr int KGB_OFF_X = KGB_OFF_AT + KGB_PAIRS * 10 * 256 * 4;       // [pairs] inverse tiles of the merge
 constexpr int KGB_X_FLOATS = 4 * XTS + 4 * XRS;
@@ -122,6 +126,7 @@ constexpr int KGB_BYTES = KGB_OFF_SC + 2 * 64 * 4 + 1024;      // + alignment sl
 static_assert(KGB_OFF_STEEP + 8 * 4 * 4 <= KGB_OFF_OPS, "header fits");
 static_assert(KGB_OFF_OPS % 1024 == 0 && KGB_OPS_BYTES % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 static_assert(KGB_OFF_STAGE % 128 == 0 && KGB_STAGE_BYTES % 128 == 0, "TMA destinations are 128-byte aligned");
+static_assert(KGB_BYTES <= 227 * 1024, "fits the shared memory of one CTA");
 
 constexpr uint32_t KGB_TMEM_COLS = 512;            // the whole TMEM of the SM (one CTA per SM)
 constexpr uint32_t KGB_IDESC = tc::idesc_tf32<128, 128>();
@@ -210,19 +215,29 @@ __device__ __forceinline__ void load4(const unsigned char *row, int c, const T16
     for (int i = 0; i < 4; ++i) v[i] = float(h[i]);
 }
 
-__device__ __forceinline__ void split4(const float (&v)[4], uint4 &hi, uint4 &lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) split_tf32(v[i], h[i], l[i]);
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
+// TF32 split of two values at once: hi truncated to TF32 (explicitly, so that
+// hi + lo is the value whatever the tensor core does with low mantissa bits),
+// lo = v - hi exactly (FP32 subtraction of numbers that share their top bits);
+// the tensor core reads lo as TF32, an error of at most 2^-11 |lo| <= 2^-22 |v|.
+__device__ __forceinline__ void split2(float2 v, uint32_t &h0, uint32_t &h1, uint32_t &l0, uint32_t &l1) {
+    h0 = __float_as_uint(v.x) & 0xffffe000u;
+    h1 = __float_as_uint(v.y) & 0xffffe000u;
+    const float2 lo = __fadd2_rn(v, make_float2(-__uint_as_float(h0), -__uint_as_float(h1)));
+    l0 = __float_as_uint(lo.x);
+    l1 = __float_as_uint(lo.y);
 }
 
 // Slice in the staging slot -> the four operand parts in the swizzled buffer
 // `ops` (A rows 0-63 Qh, 64-127 Ql; B rows 0-63 Ph, 64-127 Pl).  Transform
 // thread tt (0 .. KGB_TTHREADS - 1; KGB_TTHREADS a multiple of 8) handles
-// channels 4 (tt & 7) .. + 3 of rows (tt + KGB_TTHREADS v) >> 3.  Returns this thread's 4-bit mask of channels
-// left out as steep.
+// channels 4 (tt & 7) .. + 3 of rows (tt + KGB_TTHREADS v) >> 3.  Returns this
+// thread's 4-bit mask of channels left out as steep.
+//
+// Rows at or past the chunk's end are transformed like live rows: whatever they
+// hold (zeros past the tensor's end, the next request's tokens), they only reach
+// accumulator rows i >= n and columns j >= n, which the epilogue's strict-lower
+// and live-row selects discard.  Pairs of values go through the paired FP32
+// instructions (each half rounds exactly like its scalar form).
 template <typename TIn>
 __device__ __forceinline__ uint32_t kgb_tc_transform(const unsigned char *stage, unsigned char *ops, int n,
                                                      int tt) {
@@ -238,34 +253,44 @@ __device__ __forceinline__ uint32_t kgb_tc_transform(const unsigned char *stage,
     load4(gb, c, (const float *)nullptr, gfirst);
     load4(gb + (n - 1) * 128, c, (const float *)nullptr, glast);
     uint32_t steep = 0;
-    bool keep[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float up = (gfirst[i] - ref[i]) * LH, dn = (ref[i] - glast[i]) * LH;
-        keep[i] = up <= SAFE2 && dn <= SAFE2;          // false for NaN too
-        steep |= keep[i] ? 0u : (1u << i);
+        const bool keep = up <= SAFE2 && dn <= SAFE2;   // false for NaN too
+        steep |= keep ? 0u : (1u << i);
     }
+    const float2 nref01 = make_float2(-ref[0], -ref[1]), nref23 = make_float2(-ref[2], -ref[3]);
+    const float2 lh2 = make_float2(LH, LH);
     static_assert(KGB_TTHREADS % 8 == 0, "a thread keeps its channel group");
 #pragma unroll
     for (int v = 0; v < (64 * 8 + KGB_TTHREADS - 1) / KGB_TTHREADS; ++v) {
         if (tt + KGB_TTHREADS * v >= 64 * 8) break;
         const int r = (tt + KGB_TTHREADS * v) >> 3;
-        float kv[4], gv[4], q[4], pp[4];
+        float kv[4], gv[4];
         load4(kb + r * KP, c, (const TIn *)nullptr, kv);
         load4(gb + r * 128, c, (const float *)nullptr, gv);
-        const bool live = r < n;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            // the exponent (g - ref) log2 e: the difference is taken first, so its
-            // error does not grow with |g|
-            const float e = (gv[i] - ref[i]) * LH;
-            const bool on = live && keep[i];           // selected after: 0 * inf would be NaN
-            q[i] = on ? kv[i] * ex2(e) : 0.f;
-            pp[i] = on ? kv[i] * ex2(-e) : 0.f;
+        // the exponent (g - ref) log2 e: the difference is taken first, so its
+        // error does not grow with |g|
+        float2 e01 = __fmul2_rn(__fadd2_rn(make_float2(gv[0], gv[1]), nref01), lh2);
+        float2 e23 = __fmul2_rn(__fadd2_rn(make_float2(gv[2], gv[3]), nref23), lh2);
+        float2 k01 = make_float2(kv[0], kv[1]), k23 = make_float2(kv[2], kv[3]);
+        if (steep != 0u) {
+            // a steep channel enters the product as zeros: key 0, exponent 0
+            // (selected, so that no 0 * inf arises)
+            if (steep & 1u) k01.x = e01.x = 0.f;
+            if (steep & 2u) k01.y = e01.y = 0.f;
+            if (steep & 4u) k23.x = e23.x = 0.f;
+            if (steep & 8u) k23.y = e23.y = 0.f;
         }
+        const float2 q01 = __fmul2_rn(k01, make_float2(ex2(e01.x), ex2(e01.y)));
+        const float2 q23 = __fmul2_rn(k23, make_float2(ex2(e23.x), ex2(e23.y)));
+        const float2 p01 = __fmul2_rn(k01, make_float2(ex2(-e01.x), ex2(-e01.y)));
+        const float2 p23 = __fmul2_rn(k23, make_float2(ex2(-e23.x), ex2(-e23.y)));
         uint4 qh, ql, ph, pl;
-        split4(q, qh, ql);
-        split4(pp, ph, pl);
+        split2(q01, qh.x, qh.y, ql.x, ql.y);
+        split2(q23, qh.z, qh.w, ql.z, ql.w);
+        split2(p01, ph.x, ph.y, pl.x, pl.y);
+        split2(p23, ph.z, ph.w, pl.z, pl.w);
         const int sw = 16 * (c ^ (r & 7));             // swizzled chunk position (rows r and 64 + r alike)
         *reinterpret_cast<uint4 *>(A + r * 128 + sw) = qh;
         *reinterpret_cast<uint4 *>(A + (64 + r) * 128 + sw) = ql;
@@ -409,9 +434,11 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
             mbar_init(&bars[BAR_ST_FULL + b], 1);
             mbar_init(&bars[BAR_ST_EMPTY + b], KGB_TWARPS);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < KGB_NOPS; ++b) {
             mbar_init(&bars[BAR_OPS_FULL + b], KGB_TWARPS);
             mbar_init(&bars[BAR_OPS_EMPTY + b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(&bars[BAR_D_FULL + b], 2);
             mbar_init(&bars[BAR_D_EMPTY + b], 4);
         }
@@ -458,8 +485,8 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
                 // the accumulator buffer's previous chunk-head has been read out
                 ok = kgb_wait(bars, BAR_D_EMPTY + db, ((mc >> 1) & 1) ^ 1, p.err);
                 for (int ms = 0; ok && ms < nsl; ++ms, ++mu) {
-                    const int ob = mu & 1;
-                    if (!(ok = kgb_wait(bars, BAR_OPS_FULL + ob, (mu >> 1) & 1, p.err))) break;
+                    const int ob = mu % KGB_NOPS;
+                    if (!(ok = kgb_wait(bars, BAR_OPS_FULL + ob, (mu / KGB_NOPS) & 1, p.err))) break;
                     tc::fence_after_sync();
                     const uint32_t a0 = smem_u32(sm + KGB_OFF_OPS + ob * KGB_OPS_BYTES), b0 = a0 + 128 * 128;
 #pragma unroll
@@ -483,9 +510,9 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
         bool ok = true;
         for (uint32_t c = 0; m.valid && ok; ++c, m = walk.next(p)) {
             for (int s = 0; s < nsl; ++s, ++u) {
-                const int slot = u % KGB_NST, ob = u & 1;
+                const int slot = u % KGB_NST, ob = u % KGB_NOPS;
                 ok = kgb_wait(bars, BAR_ST_FULL + slot, (u / KGB_NST) & 1, p.err) &&
-                     kgb_wait(bars, BAR_OPS_EMPTY + ob, ((u >> 1) & 1) ^ 1, p.err);
+                     kgb_wait(bars, BAR_OPS_EMPTY + ob, ((u / KGB_NOPS) & 1) ^ 1, p.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const uint32_t st = kgb_tc_transform<TIn>(sm + KGB_OFF_STAGE + slot * KGB_STAGE_BYTES,

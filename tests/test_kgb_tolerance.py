@@ -7,7 +7,9 @@ with one reference value c_d per channel (g of the chunk's middle live row):
   taken first and then scaled, so the exponent's error grows with its size but
   not with |g|;
 * A = beta * strict_lower(Q P^T), the product taken in split TF32 on the tensor
-  cores (Qh Ph^T + Qh Pl^T + Ql Ph^T, hi parts truncated to TF32, FP32 sums);
+  cores (Qh Ph^T + Qh Pl^T + Ql Ph^T, FP32 sums): the hi parts truncated to
+  TF32, the lo parts the exact FP32 remainders, which the tensor cores read as
+  TF32 (modelled both truncated and rounded to nearest);
 * a channel whose g leaves [c - 48, c + 48] over the chunk's live rows is left
   out of the product and its terms k_i k_j exp(g_i - g_j) are added one by one.
 
@@ -35,7 +37,14 @@ def _tf32(x):
     return (np.asarray(x, np.float32).view(np.uint32) & np.uint32(0xFFFFE000)).view(np.float32)
 
 
-def _fp32_construction(k, g, beta, n, steep_path=True):
+def _tf32_rn(x):
+    """Round float32 values to the nearest TF32 value (ties to even)."""
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0xFFF) + ((b >> np.uint64(13)) & np.uint64(1))) & np.uint64(0xFFFFE000)
+    return b.astype(np.uint32).view(np.float32)
+
+
+def _fp32_construction(k, g, beta, n, steep_path=True, lo_read=_tf32):
     """FP32 A [n, n] of one chunk-head by the single-reference factorisation."""
     f32 = np.float32
     k = k.astype(f32)
@@ -49,7 +58,7 @@ def _fp32_construction(k, g, beta, n, steep_path=True):
         Q = np.where(keep, k * np.exp2(e), 0).astype(f32)
         P = np.where(keep, k * np.exp2(-e), 0).astype(f32)
         Qh, Ph = _tf32(Q), _tf32(P)
-        Ql, Pl = _tf32(Q - Qh), _tf32(P - Ph)
+        Ql, Pl = lo_read((Q - Qh).astype(f32)), lo_read((P - Ph).astype(f32))
         D = (Qh.astype(np.float64) @ Ph.T.astype(np.float64) + Qh.astype(np.float64) @ Pl.T.astype(np.float64)
              + Ql.astype(np.float64) @ Ph.T.astype(np.float64)).astype(f32)
         for dch in np.nonzero(~keep)[0]:
@@ -90,9 +99,18 @@ def _worst(kind, in_dtype, **kw):
 
 @pytest.mark.parametrize("kind", ["kda", "nodecay", "steep"])
 @pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
-def test_fp32_construction_is_far_inside_the_tolerance(kind, in_dtype):
-    worst = _worst(kind, in_dtype)
+@pytest.mark.parametrize("lo_read", [_tf32, _tf32_rn], ids=["lo_truncated", "lo_rounded"])
+def test_fp32_construction_is_far_inside_the_tolerance(kind, in_dtype, lo_read):
+    worst = _worst(kind, in_dtype, lo_read=lo_read)
     assert worst <= 2e-5 / 100, worst
+
+
+def test_tf32_rounding_helpers():
+    x = np.array([1.0, 1.0 + 2.0 ** -10, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -12,
+                  -1.5 - 2.0 ** -11, 1.0 + 2.0 ** -11 + 2.0 ** -13], np.float32)
+    assert _tf32(x).tolist() == [1.0, 1.0 + 2.0 ** -10, 1.0, 1.0 + 2.0 ** -10, 1.0, -1.5, 1.0]
+    # ties go to the even TF32 neighbour; below half rounds down, above half up
+    assert _tf32_rn(x).tolist() == [1.0, 1.0 + 2.0 ** -10, 1.0, 1.0 + 2.0 ** -9, 1.0, -1.5, 1.0 + 2.0 ** -10]
 
 
 def test_steep_channels_need_their_slow_path():
