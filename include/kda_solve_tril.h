@@ -37,7 +37,12 @@
  * Ownership: the caller owns every buffer (A, Ai, cu_seqlens, workspace); the
  * library allocates no device memory and keeps no per-call state.  All device
  * calls are asynchronous on the given stream (a cudaStream_t passed as void*;
- * NULL = the legacy default stream) and do not synchronise the host.
+ * NULL = the legacy default stream) and do not synchronise the host.  The
+ * single-pass, short-chunk and fused kernels are launched with programmatic
+ * stream serialization (the split path's two kernels are not): one may be scheduled
+ * onto the SMs while the previous kernel of its stream finishes, but it waits
+ * for that kernel to complete, with its writes visible, before it reads or
+ * writes any global memory, so stream order holds as for ordinary launches.
  *
  * Stream capture: the first call of each entry point on a device sets up
  * per-device state (device attributes, the error word's address, kernel

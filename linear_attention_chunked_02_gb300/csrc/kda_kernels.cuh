@@ -131,6 +131,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Programmatic dependent launch (the kernels are launched with programmatic
+// stream serialization).  launch_dependents lets the next kernel of the stream be
+// scheduled onto SMs as this grid's CTAs leave; wait blocks until the previous
+// kernel of the stream has completed and its memory writes are visible, so
+// every kernel calls it before its first global memory access.  Both are no-ops
+// for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -685,6 +697,19 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     TOut *out = reinterpret_cast<TOut *>(p.out);
     const int tid = threadIdx.x;
     const int unit = tid >> 4, warp = tid >> 5;
+    pdl_launch_dependents();
+    if (tid == 0) {
+        // the tensor maps this kernel uses, into the TMA unit's descriptor cache
+        if (MODE == MODE_FUSED) {
+            prefetch_tensormap(&maps.m[4]);
+            prefetch_tensormap(&maps.m[5]);
+        } else {
+            for (int r = 0; r < 4; ++r) prefetch_tensormap(&maps.m[r]);
+        }
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    pdl_wait();                              // the previous kernel's writes (A, cu_seqlens) are visible
     // the task walk reads cu_seqlens from shared memory when it fits
     Params ps = p;
     if (p.cu != nullptr && p.nseq < CU_CAP) {
@@ -700,15 +725,6 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     TaskWalk walk(p, int32_t(blockIdx.x), G);   // thread 0's walk over the tasks it loads
 
     if (tid == 0) {
-        // the tensor maps this kernel uses, into the TMA unit's descriptor cache
-        if (MODE == MODE_FUSED) {
-            prefetch_tensormap(&maps.m[4]);
-            prefetch_tensormap(&maps.m[5]);
-        } else {
-            for (int r = 0; r < 4; ++r) prefetch_tensormap(&maps.m[r]);
-        }
-        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
         for (int s = 0; s < STAGES; ++s) issue<MODE, TIn>(ps, maps.m, walk, smem, s);
     }
     __syncthreads();

@@ -426,6 +426,7 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nsl = p.K / 32;
     const int32_t G = gridDim.x;
+    pdl_launch_dependents();
 
     if (tid == 0) {
         prefetch_tensormap(&maps.k);
@@ -448,6 +449,8 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
         }
         fence_mbar_init();
     }
+    // the previous kernel's writes are visible, and it holds no tensor memory
+    pdl_wait();
     if (warp == KGB_EW0) {                             // an epilogue warp owns the TMEM allocation
         tc::tmem_alloc(smem_u32(tmem_slot), KGB_TMEM_COLS);
         tc::tmem_relinquish();

@@ -179,6 +179,8 @@ kda_bt16_kernel(const SmallParams p) {
     const int32_t slots = gridDim.x * BT16_SLOTS;
     const int32_t q0 = blockIdx.x * BT16_SLOTS + slot;
     const int rs = p.H * 16;                 // row stride (elements); H * 16 * 16 < 2^31
+    pdl_launch_dependents();
+    pdl_wait();                              // the previous kernel's writes are visible
     const SmallParams ps = with_cached_cu(p, cu_s, tid);
     SlotWalk<16> walk(ps, q0, slots);
     // metas of the chunk-heads in the ring: m[0] is computed next
@@ -275,6 +277,8 @@ kda_bt32_kernel(const SmallParams p) {
     const int32_t slots = gridDim.x * 2;
     const int32_t q0 = blockIdx.x * 2 + warp;
     const int os = p.H * 32;
+    pdl_launch_dependents();
+    pdl_wait();                              // the previous kernel's writes are visible
     const SmallParams ps = with_cached_cu(p, cu_s, tid);
     SlotWalk<32> walk(ps, q0, slots);
     Meta m[S];
