@@ -19,29 +19,33 @@
 // that KDA's ordinary decays, about one nat per token, never take).
 //
 // FP32 accuracy on TF32 tensor cores: Q = Qh + Ql and P = Ph + Pl with Qh, Ph
-// truncated to TF32 and Ql, Pl the TF32 remainders.  The A operand of one
-// tcgen05.mma (M = 128) stacks [Qh; Ql], the B operand (N = 128) stacks
-// [Ph; Pl]; the FP32 accumulator D (128 TMEM lanes x 128 columns) then holds
-// Qh Ph^T, Qh Pl^T (rows 0-63) and Ql Ph^T (rows 64-127, columns 0-63), whose
-// sum is Q P^T to about 2^-22 relative (the dropped Ql Pl^T is the fourth
-// quadrant).  K = 128 channels take 16 instructions of K = 8.
+// truncated to TF32 and Ql, Pl the TF32 remainders, which sum to Q P^T to about
+// 2^-22 relative as Qh Ph^T + Qh Pl^T + Ql Ph^T (Ql Pl^T is dropped).  The
+// operand buffer holds rows [Qh; Ql] (A side) and [Ph; Pl] (B side); each step
+// of K = 8 channels issues three tcgen05.mma of M = 128, N = 64 into one FP32
+// accumulator (128 TMEM lanes x 64 columns): A from Qh, Qh, Ql against B from
+// Ph, Pl, Ph.  Accumulator rows 0-63 (TMEM lanes 0-63) are then Q P^T; rows
+// 64-127 multiply the 64 operand rows that follow the A start and are not read.
+// K = 128 channels take 48 instructions.
 //
 // One persistent CTA per SM, 16 warps in four roles; every role walks the
 // chunk-heads q = blockIdx.x + c * gridDim.x in the same order:
 //   * warp 0, lane 0 (loader): TMA loads of each chunk-head's k and g, one
 //     slice of 32 channels at a time, into a ring of KGB_NST staging slots;
 //   * warp 1, lane 0 (MMA issue): for every slice whose operands are ready,
-//     four tcgen05.mma of K = 8 into TMEM buffer c % 2, with tcgen05.commit
+//     twelve tcgen05.mma (four steps of K = 8) into TMEM buffer c % 2, with tcgen05.commit
 //     releasing the operand buffer and, after a chunk-head's last slice, the
 //     accumulator.  Issuing a TMA or tensor-core instruction holds the issuing
 //     warp for a while, so the two streams run on warps of their own;
-//   * warps 2-7 (transform): each slice of the staging ring into the four TF32
-//     operand parts in a 128-byte-swizzled buffer (three-slice ring); every warp
-//     signals the MMA warp on its own mbarrier arrival, without a group barrier;
-//   * warps 8-11 (epilogue): tcgen05.ld of the accumulator rows (warp w reads
-//     TMEM lanes 32 (w % 4) .. + 31), the three quadrants added, beta and the
-//     strict-lower and live-row masks applied, any steep channels' terms added,
-//     into the ten lower 16 x 16 blocks of the A tile of solve pair c % 2;
+//   * warps 2-7 and 10-11 (transform): each slice of the staging ring into the
+//     four TF32 operand parts in a 128-byte-swizzled buffer (three-slice ring);
+//     every warp signals the MMA warp on its own mbarrier arrival, without a
+//     group barrier;
+//   * warps 8-9 (epilogue): tcgen05.ld of accumulator rows 0-31 (warp 8, TMEM
+//     lanes 0-31) and 32-63 (warp 9; a warp reaches the lanes 32 (w % 4) .. + 31),
+//     beta and the strict-lower and live-row masks applied, any steep
+//     channels' terms added, into the ten lower 16 x 16 blocks of the A tile of
+//     solve pair c % 2;
 //   * warps 12-13 and 14-15 (solve pairs 0, 1): the 64-token solve of the A
 //     tile (diagonal forward substitution, two merge levels on mma.sync) for
 //     the chunk-heads c with c % 2 == pair.  The pairs share one copy of the
@@ -80,11 +84,15 @@ struct KgbMaps {
 };
 
 constexpr int KGB_THREADS = 512;
-constexpr int KGB_TWARPS = 6;                      // transform warps 2 .. 7
-constexpr int KGB_EW0 = 2 + KGB_TWARPS;            // first of the four epilogue warps
-constexpr int KGB_SW0 = KGB_EW0 + 4;               // first solve warp
+constexpr int KGB_TWARPS = 8;                      // transform warps 2 .. 7 and 10 .. 11
+constexpr int KGB_EW0 = 8;                         // epilogue warps 8, 9: TMEM lane quarters 0, 1
+constexpr int KGB_EWARPS = 2;
+constexpr int KGB_SW0 = 12;                        // first solve warp
 constexpr int KGB_PAIRS = (KGB_THREADS / 32 - KGB_SW0) / 2;   // solve pairs
 constexpr int KGB_TTHREADS = 32 * KGB_TWARPS;
+static_assert(KGB_EW0 % 4 == 0 && KGB_EWARPS == 2, "the epilogue warps reach TMEM lanes 0-63");
+// transform warp index 0 .. KGB_TWARPS - 1 of warp w (warps 2-7, then 10-11)
+__device__ __forceinline__ int kgb_twarp(int w) { return w < KGB_EW0 ? w - 2 : w - 2 - KGB_EWARPS; }
 // largest distance (nats) of g from the channel's reference over the chunk that
 // the tensor-core product takes; further channels go through the slow path
 constexpr float KGB_TC_SAFE = 48.0f;
@@ -129,7 +137,8 @@ static_assert(KGB_OFF_STAGE % 128 == 0 && KGB_STAGE_BYTES % 128 == 0, "TMA desti
 static_assert(KGB_BYTES <= 227 * 1024, "fits the shared memory of one CTA");
 
 constexpr uint32_t KGB_TMEM_COLS = 512;            // the whole TMEM of the SM (one CTA per SM)
-constexpr uint32_t KGB_IDESC = tc::idesc_tf32<128, 128>();
+constexpr uint32_t KGB_IDESC = tc::idesc_tf32<128, 64>();
+constexpr uint32_t KGB_DCOLS = 64;                 // accumulator columns per TMEM buffer
 
 // Chunk-heads q = q0, q0 + step, ... (every thread of a group walks the same sequence).
 struct KgbWalk {
@@ -441,10 +450,10 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars[BAR_D_FULL + b], 2);
-            mbar_init(&bars[BAR_D_EMPTY + b], 4);
+            mbar_init(&bars[BAR_D_EMPTY + b], KGB_EWARPS);
         }
         for (int b = 0; b < KGB_PAIRS; ++b) {
-            mbar_init(&bars[BAR_AT_FULL + b], 4);
+            mbar_init(&bars[BAR_AT_FULL + b], KGB_EWARPS);
             mbar_init(&bars[BAR_AT_EMPTY + b], 2);
         }
         fence_mbar_init();
@@ -491,11 +500,17 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
                     const int ob = mu % KGB_NOPS;
                     if (!(ok = kgb_wait(bars, BAR_OPS_FULL + ob, (mu / KGB_NOPS) & 1, p.err))) break;
                     tc::fence_after_sync();
-                    const uint32_t a0 = smem_u32(sm + KGB_OFF_OPS + ob * KGB_OPS_BYTES), b0 = a0 + 128 * 128;
+                    // Qh, Ql (A side) and Ph, Pl (B side): 64 rows of 128 bytes each
+                    const uint32_t qh = smem_u32(sm + KGB_OFF_OPS + ob * KGB_OPS_BYTES), ql = qh + 64 * 128;
+                    const uint32_t ph = qh + 128 * 128, pl = ph + 64 * 128;
+                    const uint32_t d = tmem + db * KGB_DCOLS;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_tf32(tmem + db * 128, tc::sw128_desc(a0 + 32 * kk), tc::sw128_desc(b0 + 32 * kk),
-                                     KGB_IDESC, ms > 0 || kk > 0);
+                    for (int kk = 0; kk < 4; ++kk) {   // K = 8 channels: 32 bytes along the row
+                        tc::mma_tf32(d, tc::sw128_desc(qh + 32 * kk), tc::sw128_desc(ph + 32 * kk), KGB_IDESC,
+                                     ms > 0 || kk > 0);
+                        tc::mma_tf32(d, tc::sw128_desc(qh + 32 * kk), tc::sw128_desc(pl + 32 * kk), KGB_IDESC, true);
+                        tc::mma_tf32(d, tc::sw128_desc(ql + 32 * kk), tc::sw128_desc(ph + 32 * kk), KGB_IDESC, true);
+                    }
                     tc::commit(smem_u32(&bars[BAR_OPS_EMPTY + ob]));
                     if (ms == nsl - 1) {
                         tc::commit(smem_u32(&bars[BAR_D_FULL + db]));
@@ -504,9 +519,9 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
                 }
             }
         }
-    } else if (warp < 2 + KGB_TWARPS) {
+    } else if (warp < KGB_EW0 || (warp >= KGB_EW0 + KGB_EWARPS && warp < KGB_SW0)) {
         // --------------------------------------------------------- transform
-        const int tt = tid - 64;                       // 0 .. KGB_TTHREADS - 1
+        const int tt = 32 * kgb_twarp(warp) + lane;    // 0 .. KGB_TTHREADS - 1
         KgbWalk walk(p, blockIdx.x, G);
         Meta m = walk.next(p);
         uint32_t u = 0;
@@ -532,9 +547,9 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
                 }
             }
         }
-    } else if (warp < KGB_SW0) {
+    } else if (warp < KGB_EW0 + KGB_EWARPS) {
         // ---------------------------------------------------------- epilogue
-        const int q4 = warp & 3, et = tid - 32 * KGB_EW0;   // TMEM lane quarter (warp w: w % 4), thread 0..127
+        const int i = tid - 32 * KGB_EW0;              // chunk row of this thread = its TMEM lane, 0..63
         float *sk = reinterpret_cast<float *>(sm + KGB_OFF_SC), *sg = sk + 64;
         KgbWalk walk(p, blockIdx.x, G);
         Meta m = walk.next(p);
@@ -543,98 +558,72 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
             float *Ab = reinterpret_cast<float *>(sm + KGB_OFF_AT) + pr * 2560;
             bool ok = kgb_wait(bars, BAR_AT_EMPTY + pr, ((c / KGB_PAIRS) & 1) ^ 1, p.err);
             ok = ok && kgb_wait(bars, BAR_D_FULL + db, (c >> 1) & 1, p.err);
-            if (!named_sync_and<3, 128>(ok)) break;
+            if (!named_sync_and<3, 64>(ok)) break;
             tc::fence_after_sync();
             const uint32_t sbase = (c & 7) * 4;
             const uint32_t any_steep = (nsl > 0 ? steep_m[sbase] : 0u) | (nsl > 1 ? steep_m[sbase + 1] : 0u) |
                                        (nsl > 2 ? steep_m[sbase + 2] : 0u) | (nsl > 3 ? steep_m[sbase + 3] : 0u);
-            const uint32_t tq = tmem + db * 128 + (uint32_t(32 * q4) << 16);
-            const int i = 32 * (q4 & 1) + lane;        // chunk row of this thread
-            if (q4 >= 2) {                             // Ql Ph^T: lanes 64..127, columns 0..63
-                float v[4][16];
+            const uint32_t tq = tmem + db * KGB_DCOLS + (uint32_t(32 * (warp - KGB_EW0)) << 16);
+            float v[4][16];
 #pragma unroll
-                for (int j0 = 0; j0 < 4; ++j0) tc::ld16(tq + 16 * j0, v[j0]);
-                tc::wait_ld();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[BAR_D_EMPTY + db]);
+            for (int j0 = 0; j0 < 4; ++j0) tc::ld16(tq + 16 * j0, v[j0]);
+            tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[BAR_D_EMPTY + db]);
+            const float bi = i < m.n ? float(reinterpret_cast<const TIn *>(p.beta)[(int64_t(m.row0) + i) * p.H + m.h])
+                                     : 0.f;
 #pragma unroll
-                for (int j0 = 0; j0 < 4; ++j0)
-                    if (16 * j0 <= i)
+            for (int j0 = 0; j0 < 4; ++j0) {
+                if (16 * j0 <= i) {                    // the row's blocks left of and on the diagonal
 #pragma unroll
-                        for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4 *>(at_elem(Ab, i, 16 * j0 + e)) =
-                                make_float4(v[j0][e], v[j0][e + 1], v[j0][e + 2], v[j0][e + 3]);
-            }
-            named_sync<3, 128>();                      // partial sums in the A tile
-            if (q4 < 2) {                              // Qh Ph^T + Qh Pl^T, plus the partial
-                const float bi = i < m.n ? float(reinterpret_cast<const TIn *>(p.beta)[(int64_t(m.row0) + i) * p.H + m.h])
-                                         : 0.f;
+                    for (int e = 0; e < 16; e += 4) {
+                        float o[4];
 #pragma unroll
-                for (int j0 = 0; j0 < 4; ++j0) {
-                    float a[16], b[16];
-                    tc::ld16(tq + 16 * j0, a);
-                    tc::ld16(tq + 64 + 16 * j0, b);
-                    tc::wait_ld();
-                    if (16 * j0 <= i) {
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            float4 *dst = reinterpret_cast<float4 *>(at_elem(Ab, i, 16 * j0 + e));
-                            const float4 w = *dst;
-                            const float wv[4] = {w.x, w.y, w.z, w.w};
-                            float o[4];
-#pragma unroll
-                            for (int x = 0; x < 4; ++x) {
-                                const int j = 16 * j0 + e + x;
-                                const float sum = (a[e + x] + b[e + x]) + wv[x];
-                                o[x] = (j < i && i < m.n) ? bi * sum : 0.f;
-                            }
-                            *dst = make_float4(o[0], o[1], o[2], o[3]);
+                        for (int x = 0; x < 4; ++x) {
+                            const int j = 16 * j0 + e + x;
+                            o[x] = (j < i && i < m.n) ? bi * v[j0][e + x] : 0.f;   // select: dropped rows may be NaN
                         }
+                        *reinterpret_cast<float4 *>(at_elem(Ab, i, 16 * j0 + e)) = make_float4(o[0], o[1], o[2], o[3]);
                     }
                 }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[BAR_D_EMPTY + db]);
             }
             if (any_steep != 0u) {
                 // slow path: the steep channels' terms, k_i k_j exp(g_i - g_j), one by one
                 constexpr float L2E = 1.4426950408889634f;
                 const int64_t rs = int64_t(p.H) * p.K;
-                const int ri = et & 63, jh = et >> 6;       // row ri, columns 32 jh .. 32 jh + 31
-                float acc[32];
+                for (int jh = 0; jh < 2; ++jh) {       // columns 32 jh .. 32 jh + 31 of row i
+                    float acc[32];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) acc[x] = 0.f;
-                for (int s = 0; s < nsl; ++s) {
-                    uint32_t mask = steep_m[sbase + s];
-                    while (mask != 0u) {
-                        const int d = 32 * s + __ffs(mask) - 1;
-                        mask &= mask - 1u;
-                        named_sync<3, 128>();                // previous channel's values consumed
-                        if (et < 64) {
-                            const bool live = et < m.n;
-                            const int64_t off = (int64_t(m.row0) + et) * rs + int64_t(m.h) * p.K + d;
-                            sk[et] = live ? float(reinterpret_cast<const TIn *>(p.k)[off]) : 0.f;
-                            sg[et] = live ? p.g[off] : 0.f;
+                    for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+                    for (int s = 0; s < nsl; ++s) {
+                        uint32_t mask = steep_m[sbase + s];
+                        while (mask != 0u) {
+                            const int d = 32 * s + __ffs(mask) - 1;
+                            mask &= mask - 1u;
+                            named_sync<3, 64>();         // previous channel's values consumed
+                            const bool live = i < m.n;
+                            const int64_t off = (int64_t(m.row0) + i) * rs + int64_t(m.h) * p.K + d;
+                            sk[i] = live ? float(reinterpret_cast<const TIn *>(p.k)[off]) : 0.f;
+                            sg[i] = live ? p.g[off] : 0.f;
+                            named_sync<3, 64>();
+                            const float ki = sk[i], gi = sg[i];
+#pragma unroll
+                            for (int x = 0; x < 32; ++x) {
+                                const int j = 32 * jh + x;
+                                if (j < i) acc[x] = fmaf(ki * sk[j], ex2((gi - sg[j]) * L2E), acc[x]);
+                            }
                         }
-                        named_sync<3, 128>();
-                        const float ki = sk[ri], gi = sg[ri];
+                    }
+                    if (i < m.n) {
 #pragma unroll
                         for (int x = 0; x < 32; ++x) {
                             const int j = 32 * jh + x;
-                            if (j < ri) acc[x] = fmaf(ki * sk[j], ex2((gi - sg[j]) * L2E), acc[x]);
+                            if (j < i) *at_elem(Ab, i, j) += bi * acc[x];
                         }
                     }
                 }
-                named_sync<3, 128>();                    // the partial-sum pass is complete
-                if (ri < m.n) {
-                    const float bi = float(reinterpret_cast<const TIn *>(p.beta)[(int64_t(m.row0) + ri) * p.H + m.h]);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        const int j = 32 * jh + x;
-                        if (j < ri) *at_elem(Ab, ri, j) += bi * acc[x];
-                    }
-                }
+                named_sync<3, 64>();                     // sk, sg free for the next chunk-head
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[BAR_AT_FULL + pr]);     // releases the A tile
