@@ -130,7 +130,8 @@ constexpr int KGB_OFF_AT = KGB_OFF_STAGE + KGB_NST * KGB_STAGE_BYTES;  // [pairs
 constexpr int KGB_OFF_X = KGB_OFF_AT + KGB_PAIRS * 10 * 256 * 4;       // [pairs] inverse tiles of the merge
 constexpr int KGB_X_FLOATS = 4 * XTS + 4 * XRS;
 constexpr int KGB_OFF_SC = KGB_OFF_X + KGB_PAIRS * KGB_X_FLOATS * 4;   // slow path: one channel's k and g, 64 rows
-constexpr int KGB_BYTES = KGB_OFF_SC + 2 * 64 * 4 + 1024;      // + alignment slack
+constexpr int KGB_OFF_CU = KGB_OFF_SC + 2 * 64 * 4;              // cu_seqlens copy (packed, < CU_CAP requests)
+constexpr int KGB_BYTES = KGB_OFF_CU + CU_CAP * 4 + 1024;         // + alignment slack
 static_assert(KGB_OFF_STEEP + 8 * 4 * 4 <= KGB_OFF_OPS, "header fits");
 static_assert(KGB_OFF_OPS % 1024 == 0 && KGB_OPS_BYTES % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 static_assert(KGB_OFF_STAGE % 128 == 0 && KGB_STAGE_BYTES % 128 == 0, "TMA destinations are 128-byte aligned");
@@ -460,6 +461,13 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
     }
     // the previous kernel's writes are visible, and it holds no tensor memory
     pdl_wait();
+    // every role's task walk reads cu_seqlens from shared memory when it fits
+    KgbParams ps = p;
+    if (p.cu != nullptr && p.nseq < CU_CAP) {
+        int32_t *cs = reinterpret_cast<int32_t *>(sm + KGB_OFF_CU);
+        for (int i = tid; i <= p.nseq; i += KGB_THREADS) cs[i] = __ldg(p.cu + i);
+        ps.cu = cs;
+    }
     if (warp == KGB_EW0) {                             // an epilogue warp owns the TMEM allocation
         tc::tmem_alloc(smem_u32(tmem_slot), KGB_TMEM_COLS);
         tc::tmem_relinquish();
@@ -472,9 +480,9 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
     if (warp == 0) {
         // ------------------------------------------------- loader (lane 0)
         if (lane == 0) {
-            KgbWalk lw(p, blockIdx.x, G);
+            KgbWalk lw(ps, blockIdx.x, G);
             uint32_t lu = 0;
-            for (Meta lm = lw.next(p); lm.valid; lm = lw.next(p)) {
+            for (Meta lm = lw.next(ps); lm.valid; lm = lw.next(ps)) {
                 int ls = 0;
                 for (; ls < nsl; ++ls, ++lu) {         // slice ls into its staging slot once it is free
                     const int slot = lu % KGB_NST;
@@ -488,11 +496,11 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue (lane 0)
         if (lane == 0) {
-            KgbWalk mw(p, blockIdx.x, G);
+            KgbWalk mw(ps, blockIdx.x, G);
             uint32_t mu = 0;
             bool ok = true;
             for (uint32_t mc = 0; ok; ++mc) {
-                if (!mw.next(p).valid) break;
+                if (!mw.next(ps).valid) break;
                 const int db = mc & 1;
                 // the accumulator buffer's previous chunk-head has been read out
                 ok = kgb_wait(bars, BAR_D_EMPTY + db, ((mc >> 1) & 1) ^ 1, p.err);
@@ -522,11 +530,11 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
     } else if (warp < KGB_EW0 || (warp >= KGB_EW0 + KGB_EWARPS && warp < KGB_SW0)) {
         // --------------------------------------------------------- transform
         const int tt = 32 * kgb_twarp(warp) + lane;    // 0 .. KGB_TTHREADS - 1
-        KgbWalk walk(p, blockIdx.x, G);
-        Meta m = walk.next(p);
+        KgbWalk walk(ps, blockIdx.x, G);
+        Meta m = walk.next(ps);
         uint32_t u = 0;
         bool ok = true;
-        for (uint32_t c = 0; m.valid && ok; ++c, m = walk.next(p)) {
+        for (uint32_t c = 0; m.valid && ok; ++c, m = walk.next(ps)) {
             for (int s = 0; s < nsl; ++s, ++u) {
                 const int slot = u % KGB_NST, ob = u % KGB_NOPS;
                 ok = kgb_wait(bars, BAR_ST_FULL + slot, (u / KGB_NST) & 1, p.err) &&
@@ -551,11 +559,14 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
         // ---------------------------------------------------------- epilogue
         const int i = tid - 32 * KGB_EW0;              // chunk row of this thread = its TMEM lane, 0..63
         float *sk = reinterpret_cast<float *>(sm + KGB_OFF_SC), *sg = sk + 64;
-        KgbWalk walk(p, blockIdx.x, G);
-        Meta m = walk.next(p);
-        for (uint32_t c = 0; m.valid; ++c, m = walk.next(p)) {
+        KgbWalk walk(ps, blockIdx.x, G);
+        Meta m = walk.next(ps);
+        for (uint32_t c = 0; m.valid; ++c, m = walk.next(ps)) {
             const int pr = c % KGB_PAIRS, db = c & 1;
             float *Ab = reinterpret_cast<float *>(sm + KGB_OFF_AT) + pr * 2560;
+            // beta of row i, loaded before the waits so that its latency hides behind them
+            const float bi = i < m.n ? float(reinterpret_cast<const TIn *>(p.beta)[(int64_t(m.row0) + i) * p.H + m.h])
+                                     : 0.f;
             bool ok = kgb_wait(bars, BAR_AT_EMPTY + pr, ((c / KGB_PAIRS) & 1) ^ 1, p.err);
             ok = ok && kgb_wait(bars, BAR_D_FULL + db, (c >> 1) & 1, p.err);
             if (!named_sync_and<3, 64>(ok)) break;
@@ -571,8 +582,6 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[BAR_D_EMPTY + db]);
-            const float bi = i < m.n ? float(reinterpret_cast<const TIn *>(p.beta)[(int64_t(m.row0) + i) * p.H + m.h])
-                                     : 0.f;
 #pragma unroll
             for (int j0 = 0; j0 < 4; ++j0) {
                 if (16 * j0 <= i) {                    // the row's blocks left of and on the diagonal
@@ -631,7 +640,7 @@ kda_kgb_kernel(const __grid_constant__ KgbMaps maps, const KgbParams p) {
     } else {
         // -------------------------------------------------------- solve pairs
         const int pr = (warp - KGB_SW0) >> 1, pt = tid - 32 * KGB_SW0 - 64 * pr;   // pair, thread 0..63 in it
-        kgb_pair_loop<TOut>(p, sm, bars, pr, pt);
+        kgb_pair_loop<TOut>(ps, sm, bars, pr, pt);
     }
     tc::fence_before_sync();
     __syncthreads();
