@@ -697,8 +697,15 @@ struct Maps {
                                // then 32 and 64 columns x 32 rows (single pass); 1 head
 };
 
+// CTAs per SM the registers must allow: the single pass on 16-bit input fits
+// eight in shared memory (28 KB each), on FP32 input six (36 KB)
+template <int MODE, typename TIn>
+constexpr int min_ctas() {
+    return MODE == MODE_DIAG ? 1 : (MODE == MODE_FUSED && sizeof(TIn) == 2) ? 8 : 6;
+}
+
 template <int MODE, typename TIn, typename TOut>
-__global__ void __launch_bounds__(NTHREADS, MODE == MODE_DIAG ? 1 : 6)
+__global__ void __launch_bounds__(NTHREADS, min_ctas<MODE, TIn>())
 kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     using L = Layout<MODE, TIn>;
     constexpr bool AX = L::WIDEN;            // A values exact in TF32
