@@ -66,6 +66,12 @@ def full_tensor_bytes(inp: ki.SolverInput, in_elt: int, out_elt: int) -> int:
 
 
 # ----------------------------------------------------------------- clocks
+def parse_smi_time(text: str) -> float:
+    """Seconds since the epoch of an nvidia-smi timestamp ("2026/12/03 09:40:26.123", local time)."""
+    whole, _, frac = text.strip().partition(".")
+    return time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S")) + (float("0." + frac) if frac.isdigit() else 0.0)
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
 
@@ -107,13 +113,17 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:9]))
+                rows.append((parse_smi_time(parts[0]), float(parts[1]), float(parts[2]), parts[4:9]))
             except ValueError:
                 continue
         os.unlink(self.path)
-        # one-second timestamp resolution: keep samples within the timed window +- 1 s
-        sel = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0] or rows
+        # the samples taken during the timed region; if it was too short to hold
+        # three, the window is widened (and says so)
+        window = "timed region"
+        sel = [r for r in rows if t0 <= r[0] <= t1]
+        if len(sel) < 3:
+            window = "timed region +- 0.25 s"
+            sel = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
         if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -123,7 +133,7 @@ class ClockSampler:
                 if v.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
-                "reasons": sorted(reasons), "samples": len(sel)}
+                "reasons": sorted(reasons), "samples": len(sel), "window": window}
 
 
 # -------------------------------------------------------------- peaks etc.
@@ -638,7 +648,9 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    # 20000 steps: the 8192-token solve's timed region lasts about 0.8 s, so the
+    # 50 ms clock samples fall inside it
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(ki.WORKLOADS))

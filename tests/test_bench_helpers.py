@@ -104,3 +104,43 @@ def test_source_hash_ignores_comments_only():
     c = "int f(int x) { return x + 2; }"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_smi_timestamps_keep_their_milliseconds():
+    import time
+    base = time.mktime(time.strptime("2026/12/03 09:40:26", "%Y/%m/%d %H:%M:%S"))
+    assert bench.parse_smi_time("2026/12/03 09:40:26.250") == pytest.approx(base + 0.25)
+    assert bench.parse_smi_time("2026/12/03 09:40:26") == base
+
+
+def _sampler_with(tmp_path, rows):
+    s = bench.ClockSampler(0)
+    s.proc = object()                       # as if nvidia-smi had run
+    s.path = str(tmp_path / "clocks.csv")
+    with open(s.path, "w") as f:
+        for ts, mhz, reason in rows:
+            f.write(f"{ts}, {mhz}, 2070, 500.0, 0x0, {reason}, Not Active, Not Active, Not Active\n")
+    return s
+
+
+def test_clock_summary_uses_the_timed_region(tmp_path):
+    import time
+    t = lambda s: time.strftime("%Y/%m/%d %H:%M:%S", time.localtime(1.8e9)) + s
+    t0 = bench.parse_smi_time(t(".100"))
+    rows = [(t(".000"), 1000, "Not Active"), (t(".150"), 2070, "Not Active"), (t(".200"), 2070, "Not Active"),
+            (t(".250"), 2060, "Not Active"), (t(".900"), 500, "Active")]
+    got = _sampler_with(tmp_path, rows).summary(t0, t0 + 0.2)
+    # only the three samples inside [0.1, 0.3] count: the idle one before and the
+    # slowed one after the timed region do not
+    assert got["samples"] == 3 and got["window"] == "timed region"
+    assert got["sm_mhz"] == 2070 and got["reasons"] == []
+
+
+def test_clock_summary_widens_a_short_window(tmp_path):
+    import time
+    t = lambda s: time.strftime("%Y/%m/%d %H:%M:%S", time.localtime(1.8e9)) + s
+    t0 = bench.parse_smi_time(t(".500"))
+    rows = [(t(".300"), 2070, "Not Active"), (t(".900"), 2070, "Active")]
+    got = _sampler_with(tmp_path, rows).summary(t0, t0 + 0.01)
+    assert got["window"] == "timed region +- 0.25 s" and got["samples"] == 1
+    assert got["reasons"] == []
