@@ -555,13 +555,16 @@ def run_ours(args, world, rank, local):
     nseq = 0 if cu is None else cu.numel() - 1
     out = torch.empty(A.shape, dtype=out_dtype, device=dev)
     need = kda.workspace_size(inp.B, inp.T, inp.H, nseq) if wl.bt == 64 else 0
-    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev) if wl.bt == 64 else None
+    tf32 = args.precision == "tf32"
+    if tf32 and (wl.bt != 64 or args.path == "split"):
+        raise SystemExit("--precision tf32 is the 64-token single pass")
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev) if wl.bt == 64 and not tf32 else None
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flushes_l2(inp) else None
 
     def step():
         return kda.solve_tril(A, cu, out_dtype=out_dtype, path=args.path, out=out, workspace=ws,
-                              stream=stream, return_path=True)
+                              stream=stream, return_path=True, precision=args.precision)
 
     def timed_steps(n, run):
         return timed_calls(n, run, stream, dev, flush)
@@ -597,14 +600,14 @@ def run_ours(args, world, rank, local):
     A_dev = torch.empty_like(A)
 
     def e2e_step():
-        if wl.bt == 64:
+        if wl.bt == 64 and not tf32:
             kda.solve_tril_host(A_host, Ai_host, A_dev, out, cu_host, cu_dev, ws, stream)
             return
         with torch.cuda.stream(stream):
             A_dev.copy_(A_host, non_blocking=True)
             if cu_dev is not None:
                 cu_dev.copy_(cu_host, non_blocking=True)
-            kda.solve_tril(A_dev, cu_dev, out_dtype=out_dtype, out=out, stream=stream)
+            kda.solve_tril(A_dev, cu_dev, out_dtype=out_dtype, out=out, stream=stream, precision=args.precision)
             Ai_host.copy_(out, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 200))
@@ -620,12 +623,14 @@ def run_ours(args, world, rank, local):
         return
     peak, peak_kind = hbm_peak()
     kernel = KERNEL[wl.bt] if taken == "single" else "kda_tril_kernel<MODE_MERGE>"
+    if tf32:
+        kernel = "kda_tril_kernel<MODE_FUSED, TF32>"
     achieved = alg / (ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.in_dtype, "data": "synthetic",
-        "config": config_dict(inp, taken),
+        "config": dict(config_dict(inp, taken), **({"precision": "tf32"} if tf32 else {})),
         "effective_gbs": full / (ms / 1e3) / 1e9,
         "chunk_heads_per_s": len(inp.chunks()) * inp.H / (ms / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -655,6 +660,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(ki.WORKLOADS))
     ap.add_argument("--path", default="auto", choices=["auto", "single", "split"])
+    ap.add_argument("--precision", default="ieee", choices=["ieee", "tf32"],
+                    help="tf32: the 64-token single pass with plain TF32 merge products")
     ap.add_argument("--bt", type=int, default=64, choices=[16, 32, 64],
                     help="chunk length (16 and 32: the solver's shorter branches)")
     ap.add_argument("--op", default="solve", choices=["solve", "kgb"],

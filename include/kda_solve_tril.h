@@ -101,6 +101,13 @@ typedef enum {
     KDA_PATH_SINGLE = 2           /* one kernel, no workspace */
 } kda_path_t;
 
+/* Precision mode of the merge products (the PR description lists precision
+ * modes among the solver's regression axes; see kda_solve_tril_prec). */
+typedef enum {
+    KDA_PREC_IEEE = 0,            /* FP32-accurate: split-TF32 products (the default of every entry) */
+    KDA_PREC_TF32 = 1             /* plain TF32 products: faster, about 2^-9 relative per product */
+} kda_precision_t;
+
 /* Smallest B*T (total rows) for which the selector takes the split path (the
  * minimum input length of the same PR description).  Set from GB300
  * measurements: the single-pass kernel already inverts the four diagonal
@@ -296,6 +303,27 @@ KDA_API kda_status_t kda_solve_tril_kgb(const void *k, const float *g, const voi
                                         const int32_t *cu_seqlens, int32_t num_seqs, int64_t B, int64_t T,
                                         int32_t H, int32_t K, int32_t in_dtype, int32_t out_dtype,
                                         void *stream);
+
+/*
+ * The single-pass 64-token solve in a chosen precision mode (no workspace; the
+ * split path has the FP32-accurate mode only).
+ *
+ *   precision   KDA_PREC_IEEE: exactly kda_solve_tril_ex with KDA_PATH_SINGLE.
+ *               KDA_PREC_TF32: the four diagonal 16x16 inverses as in the IEEE
+ *               mode (FP32 forward substitution), but each 16x16 merge product
+ *               as one TF32 tensor-core product: both operands truncated to
+ *               TF32 (10 explicit mantissa bits; 16-bit input is exact), FP32
+ *               accumulation.  Each product then carries a relative error of
+ *               about 2^-9 of |P| |Q| instead of about 2^-21, so the result is
+ *               not within the IEEE mode's 2e-5*(1+|ref|); its error is bounded
+ *               elementwise by 2^-6 * (|X| |L| |X| + |X| |L| |X| |L| |X|), with X
+ *               the exact inverse and L the strictly lower A.
+ *               Anything else: KDA_ERR_INVALID_ARGUMENT.
+ *   All other arguments, layouts, rules and errors: as for kda_solve_tril.
+ */
+KDA_API kda_status_t kda_solve_tril_prec(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs,
+                                         int64_t B, int64_t T, int32_t H, int32_t in_dtype, int32_t out_dtype,
+                                         int32_t precision, void *stream);
 
 /* Static description of a status code (never NULL). */
 KDA_API const char *kda_status_string(int32_t status);

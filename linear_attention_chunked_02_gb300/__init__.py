@@ -23,6 +23,7 @@ WS_TILE_BYTES = 4096
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 PATH_CODE = {"auto": 0, "split": 1, "single": 2}
 PATH_NAME = {v: k for k, v in PATH_CODE.items()}
+PRECISION_CODE = {"ieee": 0, "tf32": 1}
 
 
 class KdaError(RuntimeError):
@@ -62,7 +63,8 @@ def _stream_ptr(stream, device) -> ctypes.c_void_p:
 def solve_tril(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
                out_dtype: torch.dtype = torch.float32, path: str = "auto",
                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-               stream: Optional[torch.cuda.Stream] = None, return_path: bool = False):
+               stream: Optional[torch.cuda.Stream] = None, return_path: bool = False,
+               precision: str = "ieee"):
     """Per chunk-head inverse of (I + strict_lower(A)).
 
     A: CUDA tensor [B, T, H, bt] (float32 / bfloat16 / float16), contiguous;
@@ -72,7 +74,11 @@ def solve_tril(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
     one path only ("auto" or "single").
     workspace: optional CUDA buffer for the split path; allocated here when the
     selector would split and none is given.
+    precision: "ieee" (FP32-accurate, every path) or "tf32" (64-token chunks, the
+    single pass with plain TF32 merge products; kda_solve_tril_prec).
     """
+    if precision not in PRECISION_CODE:
+        raise ValueError(f"unknown precision {precision!r}")
     if not A.is_cuda:
         raise ValueError("A must be a CUDA tensor")
     if A.dtype not in DTYPE_CODE or out_dtype not in DTYPE_CODE:
@@ -88,6 +94,16 @@ def solve_tril(A: torch.Tensor, cu_seqlens: Optional[torch.Tensor] = None,
         out = torch.empty(A.shape, dtype=out_dtype, device=A.device)
     elif out.shape != A.shape or out.dtype != out_dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor of A's shape and out_dtype")
+    if precision == "tf32":
+        if bt != BT or path not in ("auto", "single") or workspace is not None:
+            raise ValueError("the tf32 precision mode is the 64-token single pass (no workspace)")
+        with torch.cuda.device(A.device):
+            st = lib().kda_solve_tril_prec(
+                A.data_ptr(), out.data_ptr(), cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+                nseq, B, T, H, DTYPE_CODE[A.dtype], DTYPE_CODE[out_dtype], PRECISION_CODE[precision],
+                _stream_ptr(stream, A.device))
+        _check(st, "kda_solve_tril_prec")
+        return (out, "single") if return_path else out
     if bt != BT:
         if path not in ("auto", "single") or workspace is not None:
             raise ValueError(f"{bt}-token chunks have a single path and take no workspace")

@@ -26,6 +26,8 @@ SIGNATURES = [
                                        _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     ("kda_solve_tril_split_static", _c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int64,
                                                _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_void_p]),
+    ("kda_solve_tril_prec", _c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int64, _c.c_int64,
+                                       _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_void_p]),
     ("kda_solve_tril_bt", _c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int64, _c.c_int64,
                                      _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_void_p]),
     ("kda_solve_tril_kgb", _c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32,

@@ -256,11 +256,14 @@ kda_path_t kda_solve_tril_select(int64_t B, int64_t T, int32_t H, int32_t num_se
     return KDA_PATH_SPLIT;
 }
 
-kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B,
-                               int64_t T, int32_t H, int32_t in_dtype, int32_t out_dtype, void *workspace,
-                               size_t workspace_bytes, void *stream, int32_t path, int32_t *path_taken) {
+// kda_solve_tril_ex with a precision mode (the TF32 mode exists for the single pass only)
+static kda_status_t solve_impl(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B, int64_t T,
+                        int32_t H, int32_t in_dtype, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                        void *stream, int32_t path, int32_t precision, int32_t *path_taken) {
     if (path != KDA_PATH_AUTO && path != KDA_PATH_SPLIT && path != KDA_PATH_SINGLE)
         return KDA_ERR_INVALID_ARGUMENT;
+    if (precision != KDA_PREC_IEEE && precision != KDA_PREC_TF32) return KDA_ERR_INVALID_ARGUMENT;
+    if (precision == KDA_PREC_TF32 && path != KDA_PATH_SINGLE) return KDA_ERR_INVALID_ARGUMENT;
     kda_status_t st = check_args(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype);
     if (st != KDA_OK) return st;
     const size_t need = kda_solve_tril_workspace_size(B, T, H, num_seqs);
@@ -311,9 +314,24 @@ kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *cu_seqlen
         e = dispatch(kda::MODE_DIAG, in_dtype, out_dtype, maps, p, device, info.num_sms, s);
         if (e == cudaSuccess) e = dispatch(kda::MODE_MERGE, in_dtype, out_dtype, maps, p, device, info.num_sms, s);
     } else {
-        e = dispatch(kda::MODE_FUSED, in_dtype, out_dtype, maps, p, device, info.num_sms, s);
+        e = dispatch(precision == KDA_PREC_TF32 ? kda::MODE_FUSED_TF32 : kda::MODE_FUSED, in_dtype, out_dtype, maps,
+                     p, device, info.num_sms, s);
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_solve_tril_ex(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B,
+                               int64_t T, int32_t H, int32_t in_dtype, int32_t out_dtype, void *workspace,
+                               size_t workspace_bytes, void *stream, int32_t path, int32_t *path_taken) {
+    return solve_impl(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype, workspace, workspace_bytes, stream,
+                      path, KDA_PREC_IEEE, path_taken);
+}
+
+kda_status_t kda_solve_tril_prec(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B,
+                                 int64_t T, int32_t H, int32_t in_dtype, int32_t out_dtype, int32_t precision,
+                                 void *stream) {
+    return solve_impl(A, Ai, cu_seqlens, num_seqs, B, T, H, in_dtype, out_dtype, nullptr, 0, stream,
+                      KDA_PATH_SINGLE, precision, nullptr);
 }
 
 kda_status_t kda_solve_tril(const void *A, void *Ai, const int32_t *cu_seqlens, int32_t num_seqs, int64_t B,

@@ -59,6 +59,9 @@ constexpr int CU_CAP = 256;
 constexpr int MODE_FUSED = 0;
 constexpr int MODE_DIAG = 1;
 constexpr int MODE_MERGE = 2;
+// launch selector for the single pass in the TF32 precision mode (the kernel is
+// MODE_FUSED with its TF32 template flag set)
+constexpr int MODE_FUSED_TF32 = 3;
 
 // On-chip FP32 tiles.  Widened 16-bit A blocks: pitch 16, block stride 272
 // floats.  X tiles: "Xt" slots hold transposed inverse blocks row-major with
@@ -600,30 +603,33 @@ __device__ __forceinline__ void right2(TileB &b, const float *r, int rp, int g, 
         }
 }
 
-// c += P Q in split TF32 (B_EXACT: Q has no lo part).
-template <bool B_EXACT>
+// c += P Q in split TF32 (B_EXACT: Q has no lo part).  TF32: the precision mode
+// that takes P Q as one TF32 product (Ph Qh; the lo parts are not used).
+template <bool B_EXACT, bool TF32 = false>
 __device__ __forceinline__ void mma_tile(TileC &c, const TileA &a, const TileB &b) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            mma8(c.c[nt], a.l[ks], b.h[ks][nt][0], b.h[ks][nt][1]);
-            if (!B_EXACT) mma8(c.c[nt], a.h[ks], b.l[ks][nt][0], b.l[ks][nt][1]);
+            if (!TF32) mma8(c.c[nt], a.l[ks], b.h[ks][nt][0], b.h[ks][nt][1]);
+            if (!B_EXACT && !TF32) mma8(c.c[nt], a.h[ks], b.l[ks][nt][0], b.l[ks][nt][1]);
             mma8(c.c[nt], a.h[ks], b.h[ks][nt][0], b.h[ks][nt][1]);
         }
 }
 
 // c += P Q and d += P R, interleaved (two independent accumulator chains; each
 // accumulates in the same order as mma_tile).
-template <bool B_EXACT>
+template <bool B_EXACT, bool TF32 = false>
 __device__ __forceinline__ void mma_tile2(TileC &c, TileC &d, const TileA &a, const TileB &q, const TileB &r) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            mma8(c.c[nt], a.l[ks], q.h[ks][nt][0], q.h[ks][nt][1]);
-            mma8(d.c[nt], a.l[ks], r.h[ks][nt][0], r.h[ks][nt][1]);
-            if (!B_EXACT) {
+            if (!TF32) {
+                mma8(c.c[nt], a.l[ks], q.h[ks][nt][0], q.h[ks][nt][1]);
+                mma8(d.c[nt], a.l[ks], r.h[ks][nt][0], r.h[ks][nt][1]);
+            }
+            if (!B_EXACT && !TF32) {
                 mma8(c.c[nt], a.h[ks], q.l[ks][nt][0], q.l[ks][nt][1]);
                 mma8(d.c[nt], a.h[ks], r.l[ks][nt][0], r.l[ks][nt][1]);
             }
@@ -704,7 +710,8 @@ constexpr int min_ctas() {
     return MODE == MODE_DIAG ? 1 : (MODE == MODE_FUSED && sizeof(TIn) == 2) ? 8 : 6;
 }
 
-template <int MODE, typename TIn, typename TOut>
+// TF32 (MODE_FUSED only): the precision mode, merge products in plain TF32.
+template <int MODE, typename TIn, typename TOut, bool TF32 = false>
 __global__ void __launch_bounds__(NTHREADS, min_ctas<MODE, TIn>())
 kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     using L = Layout<MODE, TIn>;
@@ -848,11 +855,11 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             left_smem(la, warp == 0 ? xt00 : xt22, XTP, g, t);
             right4a(rb, a.p, a.pitch, g, t);
             zero(c1);
-            mma_tile<AX>(c1, la, rb);
+            mma_tile<AX, TF32>(c1, la, rb);
             left_regs(la, c1);
             right2(rb, Xr + (warp == 0 ? XR_11 : XR_33) * XRS, XRP, g, t);
             zero(c2);
-            mma_tile<false>(c2, la, rb);
+            mma_tile<false, TF32>(c2, la, rb);
             if (warp == 0) {
                 smem_tile_t(Xt + XT_10 * XTS, c2, g, t);
                 out_tile_t(ob, os, m.n, 1, 0, c2, g, t);
@@ -876,17 +883,17 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             {
                 const AOff<TIn> a2 = aoff<MODE, TIn>(stage, 2, warp), a3 = aoff<MODE, TIn>(stage, 3, warp);
                 right4a(rb, a2.p, a2.pitch, g, t);
-                mma_tile<AX>(ct2, la, rb);
+                mma_tile<AX, TF32>(ct2, la, rb);
                 right4a(rb, a3.p, a3.pitch, g, t);
-                mma_tile<AX>(ct3, la, rb);
+                mma_tile<AX, TF32>(ct3, la, rb);
             }
             if (warp == 0) {                 // + X10^T A21^T, X10^T A31^T
                 left_smem(la, Xt + XT_10 * XTS, XTP, g, t);
                 const AOff<TIn> a2 = aoff<MODE, TIn>(stage, 2, 1), a3 = aoff<MODE, TIn>(stage, 3, 1);
                 right4a(rb, a2.p, a2.pitch, g, t);
-                mma_tile<AX>(ct2, la, rb);
+                mma_tile<AX, TF32>(ct2, la, rb);
                 right4a(rb, a3.p, a3.pitch, g, t);
-                mma_tile<AX>(ct3, la, rb);
+                mma_tile<AX, TF32>(ct3, la, rb);
             }
             // X_2w^T = T_2w^T (-X22)^T and the first term of X_3w^T, T_2w^T (-X32)^T,
             // as two interleaved chains; then + T_3w^T (-X33)^T
@@ -898,10 +905,10 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             right2(rb3, Xr + XR_32 * XRS, XRP, g, t);
             zero(cx);
             zero(cy);
-            mma_tile2<false>(cx, cy, la, rb, rb3);
+            mma_tile2<false, TF32>(cx, cy, la, rb, rb3);
             out_tile_t(ob, os, m.n, 2, warp, cx, g, t);
             right2(rb, Xr + XR_33 * XRS, XRP, g, t);
-            mma_tile<false>(cy, lb, rb);
+            mma_tile<false, TF32>(cy, lb, rb);
             out_tile_t(ob, os, m.n, 3, warp, cy, g, t);
         }
     }

@@ -33,7 +33,7 @@ cudaError_t launch_pdl(bool pdl, void (*fn)(Args...), unsigned grid, unsigned bl
 }
 
 // Per-device cache: opt-in shared memory set and occupancy queried once.
-template <int MODE, typename TIn, typename TOut>
+template <int MODE, typename TIn, typename TOut, bool TF32 = false>
 struct KernelInfo {
     static int blocks_per_sm(int device, cudaError_t &err) {
         static std::mutex mu;
@@ -45,7 +45,7 @@ struct KernelInfo {
             return 0;
         }
         if (cached[device] > 0) return cached[device];
-        auto fn = kda_tril_kernel<MODE, TIn, TOut>;
+        auto fn = kda_tril_kernel<MODE, TIn, TOut, TF32>;
         const int bytes = Layout<MODE, TIn>::BYTES;
         err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (err != cudaSuccess) return 0;
@@ -57,10 +57,10 @@ struct KernelInfo {
     }
 };
 
-template <int MODE, typename TIn, typename TOut>
+template <int MODE, typename TIn, typename TOut, bool TF32 = false>
 cudaError_t launch_one(const Maps &maps, const Params &p, int device, int num_sms, cudaStream_t stream) {
     cudaError_t err;
-    const int occ = KernelInfo<MODE, TIn, TOut>::blocks_per_sm(device, err);
+    const int occ = KernelInfo<MODE, TIn, TOut, TF32>::blocks_per_sm(device, err);
     if (err != cudaSuccess) return err;
     long long grid = (long long)num_sms * occ;
     if (grid > p.n_tasks) grid = p.n_tasks;
@@ -68,7 +68,7 @@ cudaError_t launch_one(const Maps &maps, const Params &p, int device, int num_sm
     // the split path's two kernels run without it: on GB300 the forced split
     // solve of 8192 tokens x 64 heads took 71.6 us back to back with it, 63.8
     // without (the single pass: 39.5 with, 41.4 without)
-    return launch_pdl(MODE == MODE_FUSED, kda_tril_kernel<MODE, TIn, TOut>, (unsigned)grid, NTHREADS,
+    return launch_pdl(MODE == MODE_FUSED, kda_tril_kernel<MODE, TIn, TOut, TF32>, (unsigned)grid, NTHREADS,
                       Layout<MODE, TIn>::BYTES, stream, maps, p);
 }
 
@@ -88,6 +88,13 @@ cudaError_t launch_in(int mode, int out_dtype, const Maps &maps, const Params &p
             case 0: return launch_one<MODE_FUSED, TIn, float>(maps, p, device, num_sms, stream);
             case 1: return launch_one<MODE_FUSED, TIn, __nv_bfloat16>(maps, p, device, num_sms, stream);
             default: return launch_one<MODE_FUSED, TIn, __half>(maps, p, device, num_sms, stream);
+        }
+    }
+    if (mode == MODE_FUSED_TF32) {
+        switch (out_dtype) {
+            case 0: return launch_one<MODE_FUSED, TIn, float, true>(maps, p, device, num_sms, stream);
+            case 1: return launch_one<MODE_FUSED, TIn, __nv_bfloat16, true>(maps, p, device, num_sms, stream);
+            default: return launch_one<MODE_FUSED, TIn, __half, true>(maps, p, device, num_sms, stream);
         }
     }
     switch (out_dtype) {

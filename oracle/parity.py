@@ -136,3 +136,60 @@ def parts(inp, limit: int):
         sub_cu = torch.tensor([c - lo for c in cu[s0:s1 + 1]], dtype=torch.int32)
         yield lo, hi - lo, inp.A[:, lo:hi], sub_cu, [(r0 - lo, n) for (r0, n) in chunks if lo <= r0 < hi]
         s0 = s1
+
+
+# ------------------------------------------------ TF32 precision mode bound
+TF32_BOUND_SCALE = 2.0 ** -6
+
+
+def tf32_bounds(A: np.ndarray, X: np.ndarray, chunks, bt: int = 64) -> np.ndarray:
+    """Elementwise error bound of the TF32 precision mode, [rows, H, bt] fp64.
+
+    A: the rounded input widened to fp64, X: the exact inverse (the oracle's), both
+    [rows, H, bt]; chunks: (row0, n) of every chunk.  In that mode every 16x16
+    merge product P Q is formed from P and Q truncated to TF32 (relative error below
+    2^-10 each) with FP32 accumulation (16 terms), so it is off by at most
+    (2^-9 + 2^-18 + 16 * 2^-24) |P| |Q| < 2^-8.9 |P| |Q|.  Every off-diagonal block of
+    X is a chain of two such products (level A: X10 = -X11 A10 X00; level B:
+    X_BL = -X_BR A_BL X_TL, whose factors X_TL and X_BR carry level A's error);
+    to first order the error is at most 2 * 2^-8.9 (|X| |L| |X|) + 4 * 2^-8.9
+    (|X| |L| |X| |L| |X|) elementwise, L the strictly lower A, which
+    2^-6 * (M + M2) covers with room for the FP32 diagonal inverses.  Structural
+    entries are not bounded here (they must be exact)."""
+    rows, H, _ = A.shape
+    out = np.zeros((rows, H, bt))
+    for row0, n in chunks:
+        if n == 0:
+            continue
+        La = np.abs(np.tril(A[row0:row0 + n, :, :n].transpose(1, 0, 2), -1))   # [H, n, n]
+        Xa = np.abs(X[row0:row0 + n, :, :n].transpose(1, 0, 2))
+        M = Xa @ La @ Xa
+        M2 = M @ La @ Xa
+        out[row0:row0 + n, :, :n] = (TF32_BOUND_SCALE * (M + M2)).transpose(1, 0, 2)
+    return out
+
+
+def check_solution_tf32(got: np.ndarray, ref: np.ndarray, A: np.ndarray, chunks, bt: int, out_dtype):
+    """TF32-mode verdict: structural entries exact, values finite and within
+    tf32_bounds() (plus the output dtype's rounding for bf16/fp16 output).
+    Returns (ok, message, worst |got - ref| / bound)."""
+    rows = got.shape[0]
+    i_in = np.full(rows, -1)
+    for row0, n in chunks:
+        i_in[row0:row0 + n] = np.arange(n)
+    cov = i_in >= 0
+    tb = tf32_bounds(A, ref, chunks, bt)
+    g, r, t, ii = got[cov], ref[cov], tb[cov], i_in[cov]
+    struct = np.broadcast_to(np.arange(bt)[None, None, :] >= ii[:, None, None], g.shape)
+    if not np.array_equal(g[struct], r[struct]):
+        return False, "structural entries differ", float("inf")
+    if not np.all(np.isfinite(g)):
+        return False, "non-finite output", float("inf")
+    want = r if out_dtype == torch.float32 else round_to(r, out_dtype)
+    tol = t + (0.0 if out_dtype == torch.float32 else ulp(r, out_dtype)) + 1e-12
+    ratio = np.abs(g - want) / tol
+    worst = float(ratio[~struct].max()) if (~struct).any() else 0.0
+    if worst > 1.0:
+        k = np.unravel_index(np.argmax(np.where(struct, 0, ratio)), ratio.shape)
+        return False, f"error {worst:.3g} x the bound at {k}: got {g[k]!r} ref {r[k]!r}", worst
+    return True, "", worst

@@ -224,3 +224,27 @@ def test_python_binding_rejects_host_tensors_and_bad_shapes(L):
     assert kda._shape(torch.zeros(2, 5, 3, 16, device="meta"), None, kda.CHUNK_LENGTHS) == (2, 5, 3, 0)
     with pytest.raises(ValueError):
         kda._shape(torch.zeros(2, 5, 3, 16, device="meta"), None)  # the 64-token entry points take 64 only
+
+
+def call_prec(L, A=16, Ai=1 << 20, cu=None, nseq=0, B=1, T=64, H=1, ind=0, outd=0, prec=1):
+    return L.kda_solve_tril_prec(A, Ai, cu, nseq, B, T, H, ind, outd, prec, None)
+
+
+def test_precision_entry_argument_errors_before_any_cuda_call(L):
+    """kda_solve_tril_prec checks the precision mode and every argument on the host
+    (without a GPU, a CUDA call would give KDA_ERR_CUDA)."""
+    assert call_prec(L, prec=2) == INVALID
+    assert call_prec(L, prec=-1) == INVALID
+    assert call_prec(L, ind=7) == UNSUPPORTED
+    assert call_prec(L, H=0) == INVALID
+    assert call_prec(L, A=8) == INVALID                        # misaligned
+    assert call_prec(L, A=1 << 20, Ai=(1 << 20) + 4096) == INVALID   # overlapping
+    assert call_prec(L, cu=4096, nseq=1, B=2) == INVALID
+    assert call_prec(L, T=0) == OK and call_prec(L, B=0, prec=0) == OK
+
+
+def test_python_precision_argument(monkeypatch):
+    import torch
+    A = torch.zeros(1, 64, 1, 64)
+    with pytest.raises(ValueError, match="unknown precision"):
+        kda.solve_tril(A, precision="fp8")
