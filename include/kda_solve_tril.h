@@ -325,6 +325,17 @@ KDA_API kda_status_t kda_solve_tril_prec(const void *A, void *Ai, const int32_t 
                                          int64_t B, int64_t T, int32_t H, int32_t in_dtype, int32_t out_dtype,
                                          int32_t precision, void *stream);
 
+/*
+ * Self-test of the device-side failure detection.  Launches one thread on
+ * `stream` that waits, with the kernels' bounded wait and a limit of limit_us
+ * microseconds, on an mbarrier that completes only if `complete` is non-zero.
+ * With complete = 0 the wait runs out, the kernel records bit 1 in the device
+ * error word and returns (about limit_us plus up to 6.4 ms later); the context
+ * stays usable.  Read the word with kda_device_error.
+ *   limit_us    1 .. 1000000, else KDA_ERR_INVALID_ARGUMENT (before any CUDA call).
+ */
+KDA_API kda_status_t kda_selftest_wait(int32_t complete, uint32_t limit_us, void *stream);
+
 /* Static description of a status code (never NULL). */
 KDA_API const char *kda_status_string(int32_t status);
 

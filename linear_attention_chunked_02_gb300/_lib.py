@@ -33,6 +33,7 @@ SIGNATURES = [
     ("kda_solve_tril_kgb", _c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32,
                                       _c.c_int64, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
                                       _c.c_void_p]),
+    ("kda_selftest_wait", _c.c_int, [_c.c_int32, _c.c_uint32, _c.c_void_p]),
     ("kda_status_string", _c.c_char_p, [_c.c_int32]),
     ("kda_device_error", _c.c_int, [_c.c_int32, _c.POINTER(_c.c_uint32)]),
     ("kda_version", _c.c_int32, []),

@@ -24,6 +24,19 @@ namespace {
 
 __device__ unsigned g_kda_err;   // device-side error word, one per device
 
+// Self-test of the kernels' failure detection (one thread): an mbarrier that
+// expects one arrival and gets it only when `complete` is set.  The bounded wait
+// must then succeed; otherwise it gives up after limit_ns and the kernel records
+// ERR_WAIT_TIMEOUT in the error word and returns, as the solver kernels do.
+__global__ void kda_wait_selftest_kernel(unsigned *err, int complete, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    kda::mbar_init(&bar, 1);
+    kda::fence_mbar_init();
+    if (complete) kda::mbar_arrive(&bar);
+    if (!kda::mbar_wait_bounded(&bar, 0, limit_ns)) atomicOr(err, kda::ERR_WAIT_TIMEOUT);
+}
+
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1 - 2 * kda::BT;
 
 int elt_size(int32_t dt) { return dt == KDA_F32 ? 4 : 2; }
@@ -550,6 +563,17 @@ kda_status_t kda_device_error(int32_t device, uint32_t *code) {
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     *code = v;
     return KDA_OK;
+}
+
+kda_status_t kda_selftest_wait(int32_t complete, uint32_t limit_us, void *stream) {
+    if (limit_us == 0 || limit_us > 1000000u) return KDA_ERR_INVALID_ARGUMENT;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+    DeviceInfo info;
+    if (device_info(device, info) != cudaSuccess) return KDA_ERR_CUDA;
+    kda_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(info.err, complete != 0,
+                                                                             uint64_t(limit_us) * 1000u);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int32_t kda_version(void) { return 100; }

@@ -165,13 +165,15 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
-// Wait for phase `parity` of `bar`; gives up after WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Wait for phase `parity` of `bar`; gives up (false) after limit_ns, checked
+// every 64 suspended tries.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
-        if ((it & 63u) == 0u && globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+        if ((it & 63u) == 0u && globaltimer() - t0 > limit_ns) return false;
     }
 }
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,

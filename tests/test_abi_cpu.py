@@ -248,3 +248,8 @@ def test_python_precision_argument(monkeypatch):
     A = torch.zeros(1, 64, 1, 64)
     with pytest.raises(ValueError, match="unknown precision"):
         kda.solve_tril(A, precision="fp8")
+
+
+def test_selftest_entry_checks_its_limit(L):
+    assert L.kda_selftest_wait(0, 0, None) == INVALID
+    assert L.kda_selftest_wait(0, 1000001, None) == INVALID
