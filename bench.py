@@ -286,18 +286,61 @@ def time_oracle(inp: ki.SolverInput, seconds: float, alg_bytes: int, max_reps: i
     return alg_bytes * reps / el / 1e9, reps, el, orc.num_threads()
 
 
+REFERENCE_BUDGET_S = 90.0       # timed seconds the reference arm aims for at any --steps
+
+
+def sample_input(inp: ki.SolverInput, units: int, heads: int) -> ki.SolverInput:
+    """The first `units` requests (packed) or batch rows (dense) of `inp`, first `heads` heads."""
+    if inp.cu_seqlens is None:
+        return ki.SolverInput(inp.workload, inp.A[:units, :, :heads].contiguous(), None, inp.seqlens[:units])
+    cu = inp.cu_seqlens[:units + 1].clone()
+    rows = int(cu[-1])
+    return ki.SolverInput(inp.workload, inp.A[:, :rows, :heads].contiguous(), cu, inp.seqlens[:units])
+
+
+def reference_sample(full, steps: int, time_of):
+    """(units, heads) of the sample a reference step solves: the full workload, or
+    halved (heads first, then requests or batch rows) while `steps` solves of it
+    would take more than REFERENCE_BUDGET_S.  time_of(units, heads) times one solve
+    of a candidate; halving stops early once it no longer pays (a solve's fixed
+    cost dominates), so the sample stays as large as that allows."""
+    units = full.B if full.cu_seqlens is None else len(full.seqlens)
+    heads = full.H
+    t = time_of(units, heads)
+    while steps * t > REFERENCE_BUDGET_S and (heads > 1 or units > 1):
+        nu, nh = (units, heads // 2) if heads > 1 else (units // 2, heads)
+        nt = time_of(nu, nh)
+        if nt > 0.75 * t:
+            break
+        units, heads, t = nu, nh, nt
+    return units, heads
+
+
 def run_reference(args, world, rank):
-    """The oracle, as it stands, on the host cores: the reference arm."""
+    """The oracle, as it stands, on the host cores: the reference arm.  Each step
+    solves a bounded sample of the workload (all of it when --steps allows), sized
+    so that the timed steps take about REFERENCE_BUDGET_S."""
     if rank != 0:
         return
     wl = ki.WORKLOADS[args.workload].with_(bt=args.bt)
-    inp = ki.build(wl)
+    full = ki.build(wl)
     ine, oute = ELT[wl.in_dtype], ELT[wl.out_dtype]
-    alg = algorithmic_bytes(inp, ine, oute)
     import oracle
     orc = oracle.get()
+    cu_of = lambda x: x.cu_seqlens.numpy() if x.cu_seqlens is not None else None
+
+    def time_of(units, heads):
+        x = sample_input(full, units, heads)
+        A64, cu = oracle.to_f64(x.A), cu_of(x)
+        t0 = time.perf_counter()
+        orc.solve_tril(A64, cu)
+        return time.perf_counter() - t0
+
+    units, heads = reference_sample(full, args.steps, time_of)
+    inp = sample_input(full, units, heads)
+    alg = algorithmic_bytes(inp, ine, oute)
     A64 = oracle.to_f64(inp.A)
-    cu = inp.cu_seqlens.numpy() if inp.cu_seqlens is not None else None
+    cu = cu_of(inp)
     for _ in range(args.warmup):
         orc.solve_tril(A64, cu)
     t0 = time.perf_counter()
@@ -306,7 +349,9 @@ def run_reference(args, world, rank):
     el = time.perf_counter() - t0
     ms = el / args.steps * 1e3
     v = alg / (ms / 1e3) / 1e9
-    sample = f"the full workload ({len(inp.chunks()) * inp.H} chunk-heads) per step, fp64 oracle"
+    what = "requests" if full.cu_seqlens is not None else "batch rows"
+    sample = (f"{len(inp.chunks()) * inp.H} of the workload's {len(full.chunks()) * full.H} chunk-heads per step "
+              f"(the first {units} {what}, first {heads} of {full.H} heads), fp64 oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -472,17 +517,41 @@ def run_ours_kgb(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def sample_kgb(x: ki.KgbInput, units: int, heads: int) -> ki.KgbInput:
+    """The first `units` requests (packed) or batch rows (dense) of `x`, first `heads` heads."""
+    if x.cu_seqlens is None:
+        cut = lambda t: t[:units, :, :heads].contiguous()
+        return ki.KgbInput(x.workload, cut(x.k), cut(x.g), cut(x.beta), None, x.seqlens[:units])
+    cu = x.cu_seqlens[:units + 1].clone()
+    rows = int(cu[-1])
+    cut = lambda t: t[:, :rows, :heads].contiguous()
+    return ki.KgbInput(x.workload, cut(x.k), cut(x.g), cut(x.beta), cu, x.seqlens[:units])
+
+
 def run_reference_kgb(args, world, rank):
-    """The oracle of the fused path, as it stands, on the host cores."""
+    """The oracle of the fused path, as it stands, on the host cores, on a bounded
+    sample per step (as run_reference)."""
     if rank != 0:
         return
     wl = ki.WORKLOADS[args.workload]
-    x = ki.build_kgb(wl)
-    alg = kgb_bytes(x, ELT[wl.in_dtype], ELT[wl.out_dtype])
+    full = ki.build_kgb(wl)
     import oracle
     orc = oracle.get()
-    k, g, b = (oracle.to_f64(t) for t in (x.k, x.g, x.beta))
-    cu = x.cu_seqlens.numpy() if x.cu_seqlens is not None else None
+    f64 = lambda y: [oracle.to_f64(t) for t in (y.k, y.g, y.beta)]
+    cu_of = lambda y: y.cu_seqlens.numpy() if y.cu_seqlens is not None else None
+
+    def time_of(units, heads):
+        y = sample_kgb(full, units, heads)
+        args_, cu = f64(y), cu_of(y)
+        t0 = time.perf_counter()
+        orc.solve_kgb(*args_, cu)
+        return time.perf_counter() - t0
+
+    units, heads = reference_sample(full, args.steps, time_of)
+    x = sample_kgb(full, units, heads)
+    alg = kgb_bytes(x, ELT[wl.in_dtype], ELT[wl.out_dtype])
+    k, g, b = f64(x)
+    cu = cu_of(x)
     for _ in range(args.warmup):
         orc.solve_kgb(k, g, b, cu)
     t0 = time.perf_counter()
@@ -491,11 +560,13 @@ def run_reference_kgb(args, world, rank):
     el = time.perf_counter() - t0
     ms = el / args.steps * 1e3
     v = alg / (ms / 1e3) / 1e9
-    sample = f"the full workload ({len(x.chunks()) * x.H} chunk-heads) per step, fp64 oracle"
+    what = "requests" if full.cu_seqlens is not None else "batch rows"
+    sample = (f"{len(x.chunks()) * x.H} of the workload's {len(full.chunks()) * full.H} chunk-heads per step "
+              f"(the first {units} {what}, first {heads} of {full.H} heads), fp64 oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": kgb_config(x),
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": kgb_config(full),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
