@@ -28,7 +28,7 @@
 // 64-127 multiply the 64 operand rows that follow the A start and are not read.
 // K = 128 channels take 48 instructions.
 //
-// One persistent CTA per SM, 16 warps in four roles; every role walks the
+// One persistent CTA per SM, 16 warps in five roles; every role walks the
 // chunk-heads q = blockIdx.x + c * gridDim.x in the same order:
 //   * warp 0, lane 0 (loader): TMA loads of each chunk-head's k and g, one
 //     slice of 32 channels at a time, into a ring of KGB_NST staging slots;
