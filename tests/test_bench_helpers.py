@@ -37,7 +37,12 @@ def test_kgb_bytes():
 
 def test_l2_flush_rule():
     small = ki.build(ki.WORKLOADS["dense_1x64_h4_f32"])
-    assert bench.flushes_l2(small)
+    assert bench.flushes_l2(small) and bench.l2_policy(small) == ("flush", 1)
+    bt16 = ki.build(ki.WORKLOADS["packed_16x512_h64_f32"].with_(bt=16))      # 67 MB
+    kind, r = bench.l2_policy(bt16)
+    fp = bench.full_tensor_bytes(bt16, 4, 4)
+    assert kind == "rotate" and (r - 1) * fp >= 2 * bench.L2_BYTES and (r - 2) * fp < 2 * bench.L2_BYTES
+    assert bench.l2_policy(ki.build(ki.WORKLOADS["packed_16x512_h64_f32"])) == ("none", 1)
     assert bench.workload_key(ki.WORKLOADS["packed_16x512_h64_f32"]) == "packed_16x512_h64_f32"
     assert bench.workload_key(ki.WORKLOADS["packed_16x512_h64_f32"].with_(bt=16)) == "packed_16x512_h64_f32_bt16"
 
