@@ -11,6 +11,7 @@ transposed operand) land outside it.
 """
 import numpy as np
 import pytest
+import torch
 
 import kda_inputs as ki
 import oracle
@@ -69,7 +70,7 @@ def _worst(kind, plant=None, in_dtype="f32"):
     for row0, n in inp.chunks():
         for h in range(inp.H):
             got[row0:row0 + n, h] = _tf32_solve(A[row0:row0 + n, h], n, plant)
-    ok, msg, worst = parity.check_solution_tf32(got, ref, A, inp.chunks(), BT, parity.torch.float32)
+    ok, msg, worst = parity.check_solution_tf32(got, ref, A, inp.chunks(), BT, torch.float32)
     return ok, worst
 
 
