@@ -10,13 +10,14 @@
 //   * One persistent CTA of 64 threads (four 16-lane "units") per resident
 //     slot; a CTA walks its chunk-heads q = blockIdx.x, blockIdx.x + grid, ...
 //     (q = chunk * H + head, so neighbouring CTAs share the chunk's token rows).
-//   * Thread 0 issues TMA tile loads (cp.async.bulk.tensor, mbarrier
-//     completion) into a 2-stage ring, so the next chunk-head is in flight
-//     while the current one is computed.  The single pass fetches two boxes,
-//     rows 0-31 x columns 0-31 and rows 32-63 x columns 0-63: exactly the
-//     128-byte lines that hold the strictly lower triangle, in two TMA
-//     instructions (issuing a TMA instruction holds up thread 0's warp, so
-//     fewer, larger boxes shorten the critical path).  FP32 input is used in
+//   * One thread (thread 0; thread 32 in the single pass on 16-bit input)
+//     issues TMA tile loads (cp.async.bulk.tensor, mbarrier completion) into a
+//     2-stage ring, so the next chunk-head is in flight while the current one
+//     is computed.  The single pass fetches two boxes, rows 0-31 x columns
+//     0-31 and rows 32-63 x columns 0-63: exactly the 128-byte lines that hold
+//     the strictly lower triangle, in two TMA instructions (issuing a TMA
+//     instruction holds up the issuer's warp, so fewer, larger boxes shorten
+//     the critical path).  FP32 input is used in
 //     place from the landing buffer; 16-bit input is widened once.
 //   * Diagonal blocks: one unit per block, one lane per column, forward
 //     substitution in registers (FP32 FMA).
@@ -320,10 +321,11 @@ __device__ __forceinline__ AOff<TIn> aoff(const unsigned char *stage, int i, int
 }
 
 // ------------------------------------------------------------ task decode
-// Per-CTA state of the walk over cu_seqlens (packed layout).
+// Per-walker state: packed layout, the current request of cu_seqlens; dense
+// layout, the current batch row.
 struct Walk {
-    int32_t s;        // current request
-    int32_t cbase;    // chunks before request s
+    int32_t s;        // current request (packed) or batch row (dense)
+    int32_t cbase;    // chunks before it
 };
 
 template <int CBT = BT>
@@ -333,14 +335,21 @@ __device__ __forceinline__ int32_t nchunks(int32_t a, int32_t b) {
 }
 
 // Chunk c, head h -> (first row, valid rows, head) for chunk length CBT; P has
-// the layout fields cu, nseq, T, cpr.  Packed: w walks cu_seqlens forward, so
-// the chunks a walker locates must not decrease.
+// the layout fields cu, nseq, T, cpr.  w walks forward (cu_seqlens, or the batch
+// rows), so the chunks a walker locates must not decrease.
 template <int CBT = BT, typename P>
 __device__ __forceinline__ Meta locate(const P &p, int32_t c, int32_t h, Walk &w) {
     Meta m{0, 0, h, 0};
     if (p.cu == nullptr) {
-        const int32_t b = c / p.cpr;
-        const int32_t cc = c - b * p.cpr;
+        // batch row w.s holds chunks w.cbase .. w.cbase + cpr - 1; the walk moves
+        // forward, dividing only when it leaves the row
+        if (c - w.cbase >= p.cpr) {
+            const int32_t d = (c - w.cbase) / p.cpr;
+            w.s += d;
+            w.cbase += d * p.cpr;
+        }
+        const int32_t b = w.s;
+        const int32_t cc = c - w.cbase;
         const int64_t t0 = int64_t(cc) * CBT;
         m.row0 = static_cast<int32_t>(int64_t(b) * p.T + t0);
         const int64_t left = p.T - t0;
@@ -472,14 +481,21 @@ __device__ __forceinline__ void zero_rows(unsigned char *stage, int n, int tid) 
 
 // ------------------------------------------------------ diagonal inverse
 // Unit-lower-triangular 16x16 inverse by forward substitution, one lane per
-// column j: x[i] = sum_{k<i} (-a[i][k]) x[k] for i > j, x[j] = 1, x[i<j] = 0.
-// Only entries of `a` (pitch ap) with k < i are used.
+// column j: x[i] = [i == j] + sum_{k<i} (-a[i][k]) x[k].  Rows above j need no
+// select: every x[k] with k < j is +0, so they come out as exact zeros and x[j]
+// as exactly 1, and the rows below j take the same FMAs in the same order.
+// SELECT = true keeps the rows at or above j by a select instead: the same
+// values for finite a, with fewer registers live.  The 32-token kernel uses it
+// (without it, it spills within its 96 registers), and so do the fused
+// construction kernel's solve warps (3 % faster with it on GB300, among 16
+// warps of 128 registers).  Only entries of `a` (pitch ap) with k < i are used.
+template <bool SELECT = false>
 __device__ __forceinline__ void diag_invert(const float *a, int ap, int j, float (&x)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
     for (int i = 1; i < 16; ++i) {
-        float s = 0.f;
+        float s = SELECT ? 0.f : x[i];
 #pragma unroll
         for (int kq = 0; kq < (i + 3) / 4; ++kq) {
             const float4 v = *reinterpret_cast<const float4 *>(a + i * ap + 4 * kq);
@@ -488,7 +504,7 @@ __device__ __forceinline__ void diag_invert(const float *a, int ap, int j, float
             if (4 * kq + 2 < i) s = fmaf(-v.z, x[4 * kq + 2], s);
             if (4 * kq + 3 < i) s = fmaf(-v.w, x[4 * kq + 3], s);
         }
-        x[i] = (i > j) ? s : x[i];
+        x[i] = SELECT ? ((i > j) ? s : x[i]) : s;
     }
 }
 
@@ -643,6 +659,18 @@ __device__ __forceinline__ void mma_tile2(TileC &c, TileC &d, const TileA &a, co
 // C tile holding Y^T -> output block (bi, bj) of the chunk (rows below n only).
 template <int CBT = BT, typename TOut>
 __device__ __forceinline__ void out_tile_t(TOut *ob, int os, int n, int bi, int bj, const TileC &c, int g, int t) {
+    if (CBT == BT && n == CBT) {             // a full 64-token chunk: no row test
+        TOut *base = ob + ((16 * bi + 2 * t) * os + 16 * bj + g);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                TOut *row = base + (8 * nt + e) * os;
+                put1(row, c.c[nt][e]);
+                put1(row + 8, c.c[nt][2 + e]);
+            }
+        return;
+    }
     const bool full = n == CBT;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -727,8 +755,12 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     TOut *out = reinterpret_cast<TOut *>(p.out);
     const int tid = threadIdx.x;
     const int unit = tid >> 4, warp = tid >> 5;
+    // the thread that issues the loads (and owns the walk): warp 1's first for
+    // the single pass on 16-bit input, whose level B gives warp 1 the lighter
+    // share (measured 0.5-0.8 % faster there, 2 % slower on FP32 input)
+    constexpr int ISSUER = MODE == MODE_FUSED && AX ? 32 : 0;
     pdl_launch_dependents();
-    if (tid == 0) {
+    if (tid == ISSUER) {
         // the tensor maps this kernel uses, into the TMA unit's descriptor cache
         if (MODE == MODE_FUSED) {
             prefetch_tensormap(&maps.m[4]);
@@ -752,9 +784,9 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     const int lane = tid & 31, g = lane >> 2, t = lane & 3;   // mma fragment coordinates
     const int32_t G = gridDim.x;
     const int os = p.H * BT;                 // output row stride (elements)
-    TaskWalk walk(p, int32_t(blockIdx.x), G);   // thread 0's walk over the tasks it loads
+    TaskWalk walk(p, int32_t(blockIdx.x), G);   // the issuer's walk over the tasks it loads
 
-    if (tid == 0) {
+    if (tid == ISSUER) {
         for (int s = 0; s < STAGES; ++s) issue<MODE, TIn>(ps, maps.m, walk, smem, s);
     }
     __syncthreads();
@@ -766,7 +798,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         if (__syncthreads_or(!ok)) {
             // A copy never completed.  Record it, give the copies still in
             // flight a bounded chance to land, and stop.
-            if (tid == 0) {
+            if (tid == ISSUER) {
                 atomicOr(p.err, ERR_WAIT_TIMEOUT);
                 mbar_wait_bounded(&bars[st], parity);
                 for (int s = 1; s < STAGES; ++s)
@@ -781,7 +813,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
         // Every thread is past the previous chunk-head, so the stage it used,
         // (it - 1) % STAGES, is free: refill it with the chunk-head STAGES - 1
         // iterations ahead (the prologue issued iterations 0 .. STAGES - 1).
-        if (it >= 1 && tid == 0) {
+        if (it >= 1 && tid == ISSUER) {
             fence_proxy_async();
             issue<MODE, TIn>(ps, maps.m, walk, smem, (it + STAGES - 1) % STAGES);
         }
@@ -821,11 +853,15 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             float x[16];
             const int b = unit;
             const AView a = adiag<MODE, TIn>(stage, Af, b);
-            diag_invert(a.p, a.pitch, l, x);
+            diag_invert<!AX>(a.p, a.pitch, l, x);   // the select form for FP32 input (more registers live there)
+            TOut *op = ob + (16 * b * os + 16 * b + l);   // diagonal block of the output, lane = column
+            if (m.n == BT) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {   // diagonal block of the output, lane = column
-                const int r = 16 * b + i;
-                if (r < m.n) put1(ob + (r * os + 16 * b + l), x[i]);
+                for (int i = 0; i < 16; ++i, op += os) put1(op, x[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i, op += os)
+                    if (16 * b + i < m.n) put1(op, x[i]);
             }
             if (MODE == MODE_DIAG) {         // workspace: X_bb^T row-major, lane = row
                 float4 *w = reinterpret_cast<float4 *>(p.ws + size_t(q) * 1024 + b * 256 + l * 16);

@@ -321,7 +321,7 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
     {
         float x[16];
         const int b = unit;
-        diag_invert(Ab + blk(b, b) * 256, 16, l, x);
+        diag_invert<true>(Ab + blk(b, b) * 256, 16, l, x);   // the select form: fewer live registers
         TOut *op = ob + (16 * b * os + 16 * b + l);    // diagonal block, lane = column
         if (n == BT) {
 #pragma unroll

@@ -309,7 +309,7 @@ kda_bt32_kernel(const SmallParams p) {
                 d = af[warp] + (half ? 256 : 0);
             }
             float x[16];
-            diag_invert(d, 16, l, x);
+            diag_invert<true>(d, 16, l, x);
             TOut *op = ob + (16 * half * os + 16 * half + l);   // diagonal block, lane = column
             if (n == 32) {
 #pragma unroll
