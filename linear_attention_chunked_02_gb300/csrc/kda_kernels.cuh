@@ -74,6 +74,16 @@ constexpr int ABS = 272;
 constexpr int XTP = 16, XTS = 256;     // Xt pitch / slot stride (floats)
 constexpr int XRP = 24, XRS = 384;     // Xr pitch / slot stride (floats)
 
+// Shared-memory swizzles of rows of 16 floats (four 16-byte chunks; chunk c of
+// row r stored at c ^ swz(r)), so that the 16-byte accesses of a quarter-warp
+// fall in distinct banks.  Xt (16-bit input, and the fused construction
+// kernel's solve): a lane writing row l of a transposed inverse puts its four
+// chunks at distinct banks from its neighbours', and the MMA fragment reads
+// (rows g, g + 1 of a quarter-warp) stay conflict-free.  Widened A blocks: the
+// two 16-byte stores of each widening lane land on distinct banks across rows.
+__host__ __device__ constexpr int xt_swz(int r) { return (r >> 1) & 3; }
+__host__ __device__ constexpr int af_swz(int r) { return (r >> 1) & 1; }
+
 __host__ __device__ constexpr int blk(int i, int j) { return i * (i + 1) / 2 + j; }
 
 // Xt slots: X00^T, X22^T, X11^T, X10^T.  Xr slots: -X11, -X33, -X22, -X32.
@@ -456,9 +466,11 @@ __device__ __forceinline__ void widen_diag(const unsigned char *stage, float *Af
         float f[VEC];
         Elt<TIn>::widen(raw, f);
         const bool keep = 16 * b + i < n;
-        float *dst = Af + b * ABS + i * AP16 + k;
-        *reinterpret_cast<float4 *>(dst) = keep ? make_float4(f[0], f[1], f[2], f[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(dst + 4) = keep ? make_float4(f[4], f[5], f[6], f[7]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float *row = Af + b * ABS + i * AP16;
+        *reinterpret_cast<float4 *>(row + 4 * ((k >> 2) ^ af_swz(i))) =
+            keep ? make_float4(f[0], f[1], f[2], f[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(row + 4 * (((k >> 2) + 1) ^ af_swz(i))) =
+            keep ? make_float4(f[4], f[5], f[6], f[7]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -489,7 +501,7 @@ __device__ __forceinline__ void zero_rows(unsigned char *stage, int n, int tid) 
 // (without it, it spills within its 96 registers), and so do the fused
 // construction kernel's solve warps (3 % faster with it on GB300, among 16
 // warps of 128 registers).  Only entries of `a` (pitch ap) with k < i are used.
-template <bool SELECT = false>
+template <bool SELECT = false, bool SWZ = false>
 __device__ __forceinline__ void diag_invert(const float *a, int ap, int j, float (&x)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
@@ -498,7 +510,7 @@ __device__ __forceinline__ void diag_invert(const float *a, int ap, int j, float
         float s = SELECT ? 0.f : x[i];
 #pragma unroll
         for (int kq = 0; kq < (i + 3) / 4; ++kq) {
-            const float4 v = *reinterpret_cast<const float4 *>(a + i * ap + 4 * kq);
+            const float4 v = *reinterpret_cast<const float4 *>(a + i * ap + 4 * (SWZ ? (kq ^ af_swz(i)) : kq));
             if (4 * kq + 0 < i) s = fmaf(-v.x, x[4 * kq + 0], s);
             if (4 * kq + 1 < i) s = fmaf(-v.y, x[4 * kq + 1], s);
             if (4 * kq + 2 < i) s = fmaf(-v.z, x[4 * kq + 2], s);
@@ -548,10 +560,20 @@ __device__ __forceinline__ void zero(TileC &c) {
         for (int i = 0; i < 4; ++i) c.c[nt][i] = 0.f;
 }
 
-// Left operand (kperm4): row-major 16x16 tile at p with pitch lp.
+// Left operand (kperm4): row-major 16x16 tile at p with pitch lp.  SWZ: the
+// tile's 16-byte chunks are stored swizzled, chunk c of row r at c ^ xt_swz(r)
+// (rows g and g + 8 share the swizzle).
+template <bool SWZ = false>
 __device__ __forceinline__ void left_smem(TileA &a, const float *p, int lp, int g, int t) {
-    const float4 r0 = *reinterpret_cast<const float4 *>(p + g * lp + 4 * t);
-    const float4 r1 = *reinterpret_cast<const float4 *>(p + (g + 8) * lp + 4 * t);
+    float4 r0, r1;
+    if (SWZ) {
+        const int tc = 4 * (t ^ xt_swz(g));
+        r0 = *reinterpret_cast<const float4 *>(p + g * lp + tc);
+        r1 = *reinterpret_cast<const float4 *>(p + (g + 8) * lp + tc);
+    } else {
+        r0 = *reinterpret_cast<const float4 *>(p + g * lp + 4 * t);
+        r1 = *reinterpret_cast<const float4 *>(p + (g + 8) * lp + 4 * t);
+    }
     split_tf32(r0.x, a.h[0][0], a.l[0][0]); split_tf32(r1.x, a.h[0][1], a.l[0][1]);
     split_tf32(r0.y, a.h[0][2], a.l[0][2]); split_tf32(r1.y, a.h[0][3], a.l[0][3]);
     split_tf32(r0.z, a.h[1][0], a.l[1][0]); split_tf32(r1.z, a.h[1][1], a.l[1][1]);
@@ -685,12 +707,20 @@ __device__ __forceinline__ void out_tile_t(TOut *ob, int os, int n, int bi, int 
         }
 }
 
-// C tile holding Y^T -> Y^T row-major (pitch XTP) in shared memory.
+// C tile holding Y^T -> Y^T row-major (pitch XTP) in shared memory (SWZ: the
+// chunks swizzled as left_smem<true> reads them).
+template <bool SWZ = false>
 __device__ __forceinline__ void smem_tile_t(float *dst, const TileC &c, int g, int t) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        *reinterpret_cast<float2 *>(dst + g * XTP + 8 * nt + 2 * t) = make_float2(c.c[nt][0], c.c[nt][1]);
-        *reinterpret_cast<float2 *>(dst + (g + 8) * XTP + 8 * nt + 2 * t) = make_float2(c.c[nt][2], c.c[nt][3]);
+        if (SWZ) {
+            const int col = 4 * ((2 * nt + (t >> 1)) ^ xt_swz(g)) + 2 * (t & 1);
+            *reinterpret_cast<float2 *>(dst + g * XTP + col) = make_float2(c.c[nt][0], c.c[nt][1]);
+            *reinterpret_cast<float2 *>(dst + (g + 8) * XTP + col) = make_float2(c.c[nt][2], c.c[nt][3]);
+        } else {
+            *reinterpret_cast<float2 *>(dst + g * XTP + 8 * nt + 2 * t) = make_float2(c.c[nt][0], c.c[nt][1]);
+            *reinterpret_cast<float2 *>(dst + (g + 8) * XTP + 8 * nt + 2 * t) = make_float2(c.c[nt][2], c.c[nt][3]);
+        }
     }
 }
 
@@ -746,6 +776,9 @@ __global__ void __launch_bounds__(NTHREADS, min_ctas<MODE, TIn>())
 kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
     using L = Layout<MODE, TIn>;
     constexpr bool AX = L::WIDEN;            // A values exact in TF32
+    // 16-bit input: the Xt tiles (and the split path's workspace tiles) are
+    // swizzled; FP32 input keeps them plain (measured 1 % slower swizzled)
+    constexpr bool XSW = AX;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     const Meta *metas = reinterpret_cast<const Meta *>(smem + L::OFF_META);
@@ -836,7 +869,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             for (int v = 0; v < 3; ++v) {
                 const int e = tid + NTHREADS * v;       // float4 index in blocks 1..3
                 const int b = 1 + (e >> 6), j = (e >> 2) & 15, i4 = 4 * (e & 3);
-                const float4 x = *reinterpret_cast<const float4 *>(wt + b * 256 + j * 16 + i4);
+                const float4 x = *reinterpret_cast<const float4 *>(wt + b * 256 + j * 16 + (XSW ? 4 * ((e & 3) ^ xt_swz(j)) : i4));
                 float *d = Xr + (b == 1 ? XR_11 : b == 3 ? XR_33 : XR_22) * XRS + j;
                 d[(i4 + 0) * XRP] = -x.x; d[(i4 + 1) * XRP] = -x.y;
                 d[(i4 + 2) * XRP] = -x.z; d[(i4 + 3) * XRP] = -x.w;
@@ -853,7 +886,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             float x[16];
             const int b = unit;
             const AView a = adiag<MODE, TIn>(stage, Af, b);
-            diag_invert<!AX>(a.p, a.pitch, l, x);   // the select form for FP32 input (more registers live there)
+            diag_invert<!AX, AX>(a.p, a.pitch, l, x);   // FP32 input: the select form (more registers live there); 16-bit: the widened tiles are swizzled
             TOut *op = ob + (16 * b * os + 16 * b + l);   // diagonal block of the output, lane = column
             if (m.n == BT) {
 #pragma unroll
@@ -866,13 +899,13 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             if (MODE == MODE_DIAG) {         // workspace: X_bb^T row-major, lane = row
                 float4 *w = reinterpret_cast<float4 *>(p.ws + size_t(q) * 1024 + b * 256 + l * 16);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) w[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                for (int i = 0; i < 4; ++i) w[XSW ? i ^ xt_swz(l) : i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
                 continue;
             }
             if (b != 3) {                    // X_bb^T row-major (row = lane)
                 float4 *d = reinterpret_cast<float4 *>(Xt + (b == 0 ? XT_00 : b == 1 ? XT_11 : XT_22) * XTS + l * XTP);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                for (int i = 0; i < 4; ++i) d[XSW ? i ^ xt_swz(l) : i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
             }
             if (b != 0) {                    // -X_bb row-major (column = lane)
                 float *d = Xr + (b == 1 ? XR_11 : b == 3 ? XR_33 : XR_22) * XRS + l;
@@ -890,7 +923,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             TileB rb;
             TileC c1, c2;
             const AOff<TIn> a = warp == 0 ? aoff<MODE, TIn>(stage, 1, 0) : aoff<MODE, TIn>(stage, 3, 2);
-            left_smem(la, warp == 0 ? xt00 : xt22, XTP, g, t);
+            left_smem<XSW>(la, warp == 0 ? xt00 : xt22, XTP, g, t);
             right4a(rb, a.p, a.pitch, g, t);
             zero(c1);
             mma_tile<AX, TF32>(c1, la, rb);
@@ -899,7 +932,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             zero(c2);
             mma_tile<false, TF32>(c2, la, rb);
             if (warp == 0) {
-                smem_tile_t(Xt + XT_10 * XTS, c2, g, t);
+                smem_tile_t<XSW>(Xt + XT_10 * XTS, c2, g, t);
                 out_tile_t(ob, os, m.n, 1, 0, c2, g, t);
             } else {
                 smem_tile_neg(Xr + XR_32 * XRS, c2, g, t);
@@ -917,7 +950,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
             TileC ct2, ct3, cx;
             zero(ct2);
             zero(ct3);
-            left_smem(la, warp == 0 ? xt00 : xt11, XTP, g, t);   // X00^T | X11^T
+            left_smem<XSW>(la, warp == 0 ? xt00 : xt11, XTP, g, t);   // X00^T | X11^T
             {
                 const AOff<TIn> a2 = aoff<MODE, TIn>(stage, 2, warp), a3 = aoff<MODE, TIn>(stage, 3, warp);
                 right4a(rb, a2.p, a2.pitch, g, t);
@@ -926,7 +959,7 @@ kda_tril_kernel(const __grid_constant__ Maps maps, const Params p) {
                 mma_tile<AX, TF32>(ct3, la, rb);
             }
             if (warp == 0) {                 // + X10^T A21^T, X10^T A31^T
-                left_smem(la, Xt + XT_10 * XTS, XTP, g, t);
+                left_smem<XSW>(la, Xt + XT_10 * XTS, XTP, g, t);
                 const AOff<TIn> a2 = aoff<MODE, TIn>(stage, 2, 1), a3 = aoff<MODE, TIn>(stage, 3, 1);
                 right4a(rb, a2.p, a2.pitch, g, t);
                 mma_tile<AX, TF32>(ct2, la, rb);

@@ -334,7 +334,7 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
         if (b != 3) {                                  // X_bb^T row-major (row = lane)
             float4 *d = reinterpret_cast<float4 *>(Xt + (b == 0 ? XT_00 : b == 1 ? XT_11 : XT_22) * XTS + l * XTP);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) d[i ^ xt_swz(l)] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
         }
         if (b != 0) {                                  // -X_bb row-major (column = lane)
             float *d = Xr + (b == 1 ? XR_11 : b == 3 ? XR_33 : XR_22) * XRS + l;
@@ -347,7 +347,7 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
         TileA la;
         TileB rb;
         TileC c1, c2;
-        left_smem(la, Xt + (warp == 0 ? XT_00 : XT_22) * XTS, XTP, g, t);
+        left_smem<true>(la, Xt + (warp == 0 ? XT_00 : XT_22) * XTS, XTP, g, t);
         right4<false>(rb, Ab + (warp == 0 ? blk(1, 0) : blk(3, 2)) * 256, 16, g, t);
         zero(c1);
         mma_tile<false>(c1, la, rb);
@@ -356,7 +356,7 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
         zero(c2);
         mma_tile<false>(c2, la, rb);
         if (warp == 0) {
-            smem_tile_t(Xt + XT_10 * XTS, c2, g, t);
+            smem_tile_t<true>(Xt + XT_10 * XTS, c2, g, t);
             out_tile_t(ob, os, n, 1, 0, c2, g, t);
         } else {
             smem_tile_neg(Xr + XR_32 * XRS, c2, g, t);
@@ -370,13 +370,13 @@ __device__ __forceinline__ void kgb_solve(const float *Ab, float *Xt, float *Xr,
         TileC ct2, ct3, cx;
         zero(ct2);
         zero(ct3);
-        left_smem(la, Xt + (warp == 0 ? XT_00 : XT_11) * XTS, XTP, g, t);
+        left_smem<true>(la, Xt + (warp == 0 ? XT_00 : XT_11) * XTS, XTP, g, t);
         right4<false>(rb, Ab + blk(2, warp) * 256, 16, g, t);
         mma_tile<false>(ct2, la, rb);
         right4<false>(rb, Ab + blk(3, warp) * 256, 16, g, t);
         mma_tile<false>(ct3, la, rb);
         if (warp == 0) {                               // + X10^T A21^T, X10^T A31^T
-            left_smem(la, Xt + XT_10 * XTS, XTP, g, t);
+            left_smem<true>(la, Xt + XT_10 * XTS, XTP, g, t);
             right4<false>(rb, Ab + blk(2, 1) * 256, 16, g, t);
             mma_tile<false>(ct2, la, rb);
             right4<false>(rb, Ab + blk(3, 1) * 256, 16, g, t);
