@@ -31,6 +31,9 @@
 //     (T^T = X_TL^T A_BL^T, X_BL^T = T^T (-X_BR)^T): A is then read row-major
 //     straight from the landing buffer, and each intermediate T stays in
 //     registers as the next product's left operand.  One barrier per chunk-head.
+//   * On 16-bit input the inverse tiles and the widened diagonal blocks are kept
+//     in shared memory with their 16-byte chunks swizzled by row, so that a
+//     quarter-warp's stores and fragment reads hit distinct banks.
 //   * Every output block is stored from the registers that computed it; the
 //     zero blocks above the diagonal are 16-byte vector stores.
 //   * Split path: MODE_DIAG inverts the diagonal blocks, writes them (and the
